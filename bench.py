@@ -1,0 +1,512 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 KDA hot path.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the chunk-parallel prefill of the 1M-token workload (T = 2^20, H = 16,
+d_k = d_v = 128, bf16 inputs, fp32 state) followed by the decode step that
+continues all 16 heads by one token from the prefill's final state.
+`value` is prefill tokens/s over all ranks (inputs resident in HBM); the
+decode workload (256 sequences x 32 heads, 64 chained steps) is reported
+alongside as state GB/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own copy of the workload on its own GPU
+(independent problems, no data-path collective: weak scaling); a barrier and a
+max-over-ranks of the elapsed time bracket the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from synthetic import decode_inputs, initial_state, prefill_inputs, workload  # noqa: E402
+
+NAMES = ("q", "k", "v", "log_alpha", "beta")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; barrier + max-over-ranks only)
+# ----------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+def kernel_source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "kda_gated_delta_chunked_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, files):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash(files)
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == want:
+                return {"bytes_per_launch": float(parts[2]), "scaled_from": " ".join(parts[3:])}
+    return None
+
+
+def make_events(n):
+    """Timing events, created eagerly (torch creates the CUDA event on first record)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    return evs
+
+
+# Algorithmic work per token*head at chunk C, head size d (prefill), and the
+# irreducible HBM bytes: q, k, log_alpha (d each) and v (d) and beta read once,
+# out written once, all in the input dtype.
+def prefill_units(C=64, d=128, esz=2):
+    intra_flops = C * (3 * d + 2 * d)             # triangular halves of A, P, T K~, T V, P U
+    chain_flops = 6 * d * d                        # W S, Q~ S, K^end^T U
+    in_bytes = (4 * d + 1) * esz                   # q, k, log_alpha, v, beta
+    out_bytes = d * esz
+    return intra_flops, chain_flops, in_bytes, out_bytes
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, dist: Dist):
+    import kda_gated_delta_chunked_gb300 as kda
+
+    dev = torch.device("cuda", dist.local if dist.world > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+    w = workload(args.workload)
+    T, H, D = w.total_tokens, w.num_heads, w.d_k
+
+    # --- inputs resident in HBM (generated on the device by the seeded generator)
+    x = prefill_inputs(w, device=dev)
+    s0 = x["initial_state"]
+    out = torch.empty((T, H, D), dtype=w.torch_dtype, device=dev)
+    sf = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+    desc = kda.make_desc(1, H, D, D, T, w.torch_dtype)
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    desc = kda.make_desc(1, H, D, D, T, w.torch_dtype, ws)
+    hand = decode_inputs(w if w.decode_seqs else workload(3), 0, device=dev)
+    hand = {n: hand[n][:1, :H].contiguous() for n in NAMES}       # one token for each of the H heads
+    hand_out = torch.empty((1, H, D), dtype=w.torch_dtype, device=dev)
+    ddesc = kda.make_desc(1, H, D, D, 1, w.torch_dtype)
+    import ctypes
+    ev_store = []
+
+    def step(phase=None):
+        if phase is not None:
+            arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in phase])
+            ev_store.append(arr)
+            desc.phase_events = ctypes.cast(arr, ctypes.c_void_p)
+        else:
+            desc.phase_events = None
+        rc = kda.kda_prefill(desc, x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, s0, out, sf,
+                             stream)
+        if rc:
+            raise kda.KdaError("kda_prefill", rc)
+        rc = kda.kda_decode_step(ddesc, *(hand[n] for n in NAMES), sf, hand_out, stream)
+        if rc:
+            raise kda.KdaError("kda_decode_step", rc)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    phases = [make_events(3) for _ in range(args.steps)]
+    t0, t1 = make_events(2)
+    clock = ClockSampler(dev.index)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clock.start()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(phases[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = clock.stop()
+    ms = t0.elapsed_time(t1)
+    ms_max = dist.max(ms)
+    ms_step = ms_max / args.steps
+    intra_ms = statistics.mean(p[0].elapsed_time(p[1]) for p in phases)
+    chain_ms = statistics.mean(p[1].elapsed_time(p[2]) for p in phases)
+    if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    intra_f, chain_f, in_b, out_b = prefill_units(64, D, 2 if w.dtype == "bf16" else 4)
+    units = T * H
+    state_bytes = 2 * H * D * D * 4
+    tc_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    from kda_gated_delta_chunked_gb300 import _binding
+    kinfo = {
+        "intra": {"kernel": "kda intra-chunk (a)", "ms": intra_ms, "bound": "hbm",
+                  "achieved": units * in_b / (intra_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                  "unit": "GB/s", "algorithmic_per_launch": units * in_b,
+                  "tflops": units * intra_f / (intra_ms * 1e-3) / 1e12,
+                  "files": _binding.prefill_kernel_files(w.dtype, D)["intra"]},
+        "chain": {"kernel": "kda inter-chunk (b)", "ms": chain_ms, "bound": "tensor",
+                  "achieved": units * chain_f / (chain_ms * 1e-3) / 1e12, "peak": tc_peak,
+                  "unit": "TFLOP/s", "algorithmic_per_launch": units * chain_f,
+                  "gbs": (units * out_b + state_bytes) / (chain_ms * 1e-3) / 1e9,
+                  "files": _binding.prefill_kernel_files(w.dtype, D)["chain"]},
+    }
+    dom = max(kinfo, key=lambda k: kinfo[k]["ms"])
+    kd = kinfo[dom]
+    tr = measured_traffic(dom, kd["files"])
+    roofline = {"bound": kd["bound"], "achieved": round(kd["achieved"], 2), "peak": kd["peak"],
+                "unit": kd["unit"], "frac": round(kd["achieved"] / kd["peak"], 4),
+                "traffic": None if tr is None else tr["bytes_per_launch"],
+                "kernel": kd["kernel"], "peak_source": f"{peak_src} ({'sustained' if kd['bound'] == 'tensor' else 'copy'})",
+                "algorithmic_per_launch": kd["algorithmic_per_launch"],
+                "launch_ms": round(kd["ms"], 4)}
+
+    res = {
+        "metric": "KDA prefill tokens/s (% BF16 TC peak); decode-step state GB/s (% HBM peak)",
+        "value": round(T * dist.world / (ms_step * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": f"{w.name} + decode hand-off step", "T": T, "H": H, "d_k": D, "d_v": D,
+                   "chunk": 64, "inputs": "bf16; state and accumulation fp32",
+                   "l2": "inputs (%.1f GB per step) larger than L2; no flush" % (units * (in_b + out_b) / 1e9),
+                   "parallelism": f"replicas x{dist.world} (independent problems)"},
+        "pct_bf16_tc_peak": round(units * (intra_f + chain_f) / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+        "pct_hbm_roofline": round(units * (in_b + out_b) / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "roofline": roofline,
+        "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items() if kk != "files"}
+                    for k, v in kinfo.items()},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+
+    # --- decode workload (state GB/s)
+    if not args.no_decode:
+        res["decode"] = bench_decode(kda, args, dev, stream, peaks, peak_src)
+
+    # --- end to end through the C ABI from pinned host buffers
+    if not args.no_e2e:
+        res["e2e"] = bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc)
+    del x, out, ws
+    torch.cuda.empty_cache()
+
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return res
+
+
+def bench_decode(kda, args, dev, stream, peaks, peak_src):
+    w = workload(3)
+    N, H, D = w.decode_seqs, w.num_heads, w.d_k
+    state = initial_state(w, N, device=dev)
+    steps = [decode_inputs(w, s, device=dev) for s in range(w.decode_steps)]
+    outs = torch.empty((w.decode_steps, N, H, D), dtype=w.torch_dtype, device=dev)
+    desc = kda.make_desc(N, H, D, D, N, w.torch_dtype)
+
+    def run():
+        for s in range(w.decode_steps):
+            x = steps[s]
+            rc = kda.kda_decode_step(desc, *(x[n] for n in NAMES), state, outs[s], stream)
+            if rc:
+                raise kda.KdaError("kda_decode_step", rc)
+
+    for _ in range(max(1, args.warmup)):
+        run()
+    torch.cuda.synchronize()
+    reps = max(1, args.decode_reps)
+    t0, t1 = make_events(2)
+    clock = ClockSampler(dev.index)
+    clock.start()
+    t0.record(stream)
+    for _ in range(reps):
+        run()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clock.stop()
+    ms = t0.elapsed_time(t1) / (reps * w.decode_steps)
+    state_bytes = 2 * N * H * D * D * 4
+    io_bytes = N * H * (4 * D + 1) * 2 + N * H * D * 2
+    gbs = state_bytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "metric": "decode-step state GB/s", "value": round(gbs, 1), "unit": "GB/s",
+            "steps_per_s": round(1e3 / ms, 1), "us_per_step": round(ms * 1e3, 2),
+            "total_gbs_incl_io": round((state_bytes + io_bytes) / (ms * 1e-3) / 1e9, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peak_src, "algorithmic_per_launch": state_bytes},
+            "l2": "state (%.2f GB) larger than L2; no flush" % (state_bytes / 2e9),
+            "gpu_launches": reps * w.decode_steps, "clocks": clocks}
+
+
+def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
+    """Same metric through the public C ABI with pinned HOST buffers: every step
+    copies its inputs host->device, runs prefill + the decode hand-off, and
+    reads the outputs and final state back device->host."""
+    T, H, D = w.total_tokens, w.num_heads, w.d_k
+    hx = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in NAMES}
+    for n in NAMES:
+        hx[n].copy_(x[n])
+    hs0 = torch.empty(s0.shape, dtype=s0.dtype, pin_memory=True)
+    hs0.copy_(s0)
+    hout = torch.empty((T, H, D), dtype=w.torch_dtype).pin_memory()
+    hsf = torch.empty((1, H, D, D), dtype=torch.float32).pin_memory()
+    hho = torch.empty((1, H, D), dtype=w.torch_dtype).pin_memory()
+    dx = {n: torch.empty_like(x[n]) for n in NAMES}
+    ds0 = torch.empty_like(s0)
+    dout = torch.empty((T, H, D), dtype=w.torch_dtype, device=dev)
+    dsf = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+    dho = torch.empty((1, H, D), dtype=w.torch_dtype, device=dev)
+    h2d = sum(hx[n].numel() * hx[n].element_size() for n in NAMES) + hs0.numel() * 4
+    d2h = hout.numel() * hout.element_size() + hsf.numel() * 4 + hho.numel() * hho.element_size()
+    desc.phase_events = None
+
+    def step():
+        for n in NAMES:
+            dx[n].copy_(hx[n], non_blocking=True)
+        ds0.copy_(hs0, non_blocking=True)
+        rc = kda.kda_prefill(desc, dx["q"], dx["k"], dx["v"], dx["log_alpha"], dx["beta"], None, ds0, dout,
+                             dsf, stream)
+        if rc:
+            raise kda.KdaError("kda_prefill", rc)
+        rc = kda.kda_decode_step(ddesc, *(hand[n] for n in NAMES), dsf, dho, stream)
+        if rc:
+            raise kda.KdaError("kda_decode_step", rc)
+        hout.copy_(dout, non_blocking=True)
+        hsf.copy_(dsf, non_blocking=True)
+        hho.copy_(dho, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    steps = max(1, args.e2e_steps)
+    t0, t1 = make_events(2)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - w0) / steps
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall * 1e3, 3),
+            "steps": steps, "host_buffers": "pinned"}
+
+
+def cpu_baseline(w, seconds):
+    """The fp64 oracle, as it stands, on the host cores: a bounded sample of the
+    workload (its first tokens, all heads)."""
+    import oracle
+    x = None
+    n_tok = 256
+    spent = 0.0
+    # grow the sample until one run takes a meaningful time, then take the one
+    # whose estimated cost is about `seconds`
+    while True:
+        x = prefill_inputs(w, t_range=(0, n_tok))
+        s0 = x["initial_state"]
+        t = time.perf_counter()
+        oracle.prefill(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, s0)
+        spent = time.perf_counter() - t
+        if spent >= seconds / 4 or n_tok >= w.total_tokens:
+            break
+        n_tok = min(w.total_tokens, n_tok * 4)
+    if spent < seconds / 2 and n_tok < w.total_tokens:
+        n_tok = min(w.total_tokens, int(n_tok * seconds / max(spent, 1e-3)))
+        x = prefill_inputs(w, t_range=(0, n_tok))
+        t = time.perf_counter()
+        oracle.prefill(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, x["initial_state"])
+        spent = time.perf_counter() - t
+    return {"value": round(n_tok / spent, 2), "unit": "tokens/s", "cores": oracle.default_threads(),
+            "kind": "oracle", "seconds": round(spent, 2),
+            "sample": f"first {n_tok} tokens x {w.num_heads} heads of {w.name} (fp64 recurrence, "
+                      f"threads over head x column block)"}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    import oracle
+    w = workload(args.workload)
+    n_tok = args.ref_tokens
+    chunks = [prefill_inputs(w, t_range=(i * n_tok, (i + 1) * n_tok)) for i in range(2)]
+    s0 = chunks[0]["initial_state"]
+
+    def step(i):
+        x = chunks[i % 2]
+        oracle.prefill(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, s0)
+
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t
+    value = n_tok * args.steps / el
+    return {
+        "impl": "reference",
+        "metric": "KDA prefill tokens/s (% BF16 TC peak); decode-step state GB/s (% HBM peak)",
+        "value": round(value, 2), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": f"{w.name} + decode hand-off step", "T": w.total_tokens, "H": w.num_heads,
+                   "d_k": w.d_k, "d_v": w.d_v, "chunk": 64},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.default_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: {n_tok} tokens x {w.num_heads} heads of {w.name}"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4)
+    ap.add_argument("--decode-reps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)))
+        return
+    dist = Dist()
+    try:
+        res = run_ours(args, dist)
+        if dist.rank == 0:
+            print(json.dumps(res))
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

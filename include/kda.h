@@ -1,0 +1,163 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention hot path.
+ *
+ * The operator (page "Kimi Delta Attention" deep dive, section 03, the
+ * recurrence as written in the Kimi Linear report; section 02 for the read):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t
+ *
+ * per sequence and head, with a fixed d_k x d_v state S (rows are key
+ * channels), alpha_t in (0,1]^{d_k} a per-channel decay and beta_t a scalar.
+ * It runs in the two modes of section 06 of the same page: a chunk-parallel
+ * prefill over a packed batch of variable-length sequences, and a one-token
+ * recurrent decode step that updates the state in place.  Section 07 gives the
+ * state hand-off: the final state of a prefill is the checkpoint another
+ * prefill or the decode step continues from.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Every pointer argument is a DEVICE pointer (CUDA global memory of the
+ *    current device), row-major and densely packed.  Alignment: q, k, v,
+ *    log_alpha, out, cu_seqlens and the prefill states 16 bytes; the decode
+ *    state 32 bytes; beta its element size; the workspace 256 bytes.
+ *  - Layouts: q, k, log_alpha [T_tot, H, d_k]; v, out [T_tot, H, d_v];
+ *    beta [T_tot, H]; cu_seqlens int32 [N+1]; states fp32 [N, H, d_k, d_v]
+ *    (d_v contiguous).  The decode step uses the same layouts with T_tot = N.
+ *  - dtype (KDA_F32 or KDA_BF16) applies to q, k, v, log_alpha, beta and out;
+ *    states are always fp32; all accumulation is fp32.
+ *  - alpha = exp(log_alpha) is formed inside the kernels; beta is taken as
+ *    given (already through its sigmoid).  Scaling and normalising q and k is
+ *    the caller's business.
+ *  - Supported head sizes: d_k == d_v, 64 or 128 (else KDA_ERR_UNSUPPORTED).
+ *  - The caller owns all memory.  The library never allocates or frees
+ *    device memory and never synchronises, except kda_get_device_status,
+ *    which synchronises the stream it is given.  Work is enqueued on
+ *    `stream` (NULL = the legacy default stream); buffers must stay alive
+ *    until that work completes.  Calls are re-entrant; concurrent calls on
+ *    different streams need different workspaces.
+ *  - Return codes are synchronous and report what the host can see (bad
+ *    arguments, launch failures).  Problems only the device can detect
+ *    (a malformed cu_seqlens) are written to a status word inside the
+ *    workspace and read back with kda_get_device_status.  Nothing is thrown
+ *    across the ABI.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* null / misaligned pointer, bad size, aliasing out with an input */
+    KDA_ERR_UNSUPPORTED = 2,      /* head size or dtype outside what the kernels implement */
+    KDA_ERR_CUDA = 3,             /* a CUDA launch or API call failed (see kda_last_cuda_error) */
+    KDA_ERR_TIMEOUT = 4,          /* a bounded on-device wait gave up (device status only) */
+    KDA_ERR_BAD_SEQLENS = 5,      /* cu_seqlens not 0 = c_0 <= c_1 <= ... <= c_N = T_tot (device status) */
+    KDA_ERR_WORKSPACE = 6         /* workspace missing or smaller than kda_prefill_workspace_bytes */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Problem description.  Not retained by the library after a call returns. */
+typedef struct kda_desc {
+    int32_t num_seqs;       /* N >= 0 sequences (decode: sequences advanced by one token) */
+    int32_t num_heads;      /* H >= 1 */
+    int32_t d_k;            /* key/query head size: 64 or 128 */
+    int32_t d_v;            /* value head size: must equal d_k */
+    int64_t total_tokens;   /* T_tot = cu_seqlens[N] (decode: must equal N) */
+    int32_t dtype;          /* kda_dtype of q, k, v, log_alpha, beta, out */
+    int32_t flags;          /* reserved, must be 0 */
+    void *workspace;        /* device scratch owned by the caller (prefill only), 256-byte aligned */
+    size_t workspace_bytes; /* its size in bytes */
+    void **phase_events;    /* optional timing hook (NULL: none): kda_prefill records
+                               phase_events[0] before the intra-chunk kernel,
+                               phase_events[1] between it and the inter-chunk kernel and
+                               phase_events[2] after that, each a cudaEvent_t created by
+                               the caller, on `stream` */
+} kda_desc;
+
+/*
+ * Bytes of device workspace kda_prefill needs for this description (0 for an
+ * invalid one).  The bound depends only on N, H, d and T_tot, never on the
+ * contents of cu_seqlens, so it can be sized before the lengths are known on
+ * the host.  The workspace is scratch: its contents on entry are ignored, and
+ * on exit it holds intermediate chunk data plus the device status word.
+ */
+KDA_API size_t kda_prefill_workspace_bytes(const kda_desc *desc);
+
+/*
+ * Chunk-parallel prefill over a packed batch (deep dive section 06, "chunk-
+ * parallel KDA"; variable-length batching per the FlashKDA update there).
+ *
+ *   q, k, log_alpha  [T_tot, H, d_k]   inputs, dtype `desc->dtype`
+ *   v                [T_tot, H, d_v]
+ *   beta             [T_tot, H]
+ *   cu_seqlens       int32 [N+1], device; sequence n is packed tokens
+ *                    [cu_seqlens[n], cu_seqlens[n+1]).  NULL means one
+ *                    sequence of all T_tot tokens (then N must be 1).
+ *   initial_state    fp32 [N, H, d_k, d_v] or NULL (zero state).
+ *   out              [T_tot, H, d_v], written; must not overlap any input.
+ *   final_state      fp32 [N, H, d_k, d_v] or NULL (not written).  May be the
+ *                    same pointer as initial_state (in-place continuation).
+ *                    A sequence of length 0 returns its initial state.
+ *   stream           CUDA stream for all work.
+ *
+ * Returns KDA_OK once the work is enqueued.  A malformed cu_seqlens is not
+ * seen by the host: the kernels then skip all work, leave out/final_state
+ * unspecified and record KDA_ERR_BAD_SEQLENS in the device status word.
+ */
+KDA_API int kda_prefill(const kda_desc *desc,
+                const void *q, const void *k, const void *v,
+                const void *log_alpha, const void *beta,
+                const int32_t *cu_seqlens, const float *initial_state,
+                void *out, float *final_state, kda_stream_t stream);
+
+/*
+ * One recurrent decode step for N independent sequences (deep dive section
+ * 06, "fused recurrent KDA": decay, correct and write the state in place,
+ * reading a fixed amount of memory per head).  Inputs are [N, H, *] (one
+ * token per sequence, desc->total_tokens == N); state_inout fp32
+ * [N, H, d_k, d_v] is read and overwritten in place; out [N, H, d_v].
+ * No workspace is used (desc->workspace may be NULL).
+ */
+KDA_API int kda_decode_step(const kda_desc *desc,
+                    const void *q, const void *k, const void *v,
+                    const void *log_alpha, const void *beta,
+                    float *state_inout, void *out, kda_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the device status word that the last
+ * kda_prefill on this workspace recorded: KDA_OK, KDA_ERR_BAD_SEQLENS or
+ * KDA_ERR_TIMEOUT (KDA_ERR_CUDA if the synchronisation itself failed).
+ */
+KDA_API int kda_get_device_status(const kda_desc *desc, kda_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+KDA_API const char *kda_status_string(int status);
+
+/* The cudaError_t of the last failing CUDA call made by this thread (0 if none). */
+KDA_API int kda_last_cuda_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

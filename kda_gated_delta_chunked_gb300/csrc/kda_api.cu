@@ -1,0 +1,264 @@
+// kda_api.cu -- the C ABI declared in include/kda.h: argument checks, the
+// workspace layout, the sequence-table kernel and the dispatch to kernels.
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+#include "kda_paths.h"
+
+namespace kda {
+
+static thread_local int g_last_cuda_error = 0;
+
+static int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return KDA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Sequence table: checks cu_seqlens and turns it into per-sequence chunk
+// offsets (exclusive prefix of ceil(len / kChunk)).  One CTA; no host sync.
+// ---------------------------------------------------------------------------
+constexpr int kPrepThreads = 1024;
+
+__global__ void __launch_bounds__(kPrepThreads)
+kda_sequence_table(const int32_t* __restrict__ cu_in, int N, int64_t T_tot, DeviceHeader* hdr,
+                   int32_t* __restrict__ chunk_first, int64_t chunks_ub) {
+    __shared__ int s_bad;
+    __shared__ long long s_carry;
+    __shared__ long long s_warp[kPrepThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int32_t* cu_local = hdr->pad;               // used when the caller passes no cu_seqlens
+    const int32_t* cu = cu_in;
+    if (cu_in == nullptr) {
+        if (tid == 0) { cu_local[0] = 0; cu_local[1] = (int32_t)T_tot; }
+        __syncthreads();
+        cu = cu_local;
+    }
+    if (tid == 0) {
+        s_bad = (cu[0] != 0 || (int64_t)cu[N] != T_tot) ? 1 : 0;
+        s_carry = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < N; base += kPrepThreads) {
+        const int i = base + tid;
+        long long cnt = 0;
+        if (i < N) {
+            const int32_t a = cu[i], b = cu[i + 1];
+            if (b < a) s_bad = 1;
+            else cnt = ((long long)b - a + kChunk - 1) / kChunk;
+        }
+        long long x = cnt;                       // inclusive warp scan
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            long long w = s_warp[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                long long y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            s_warp[lane] = w;                    // inclusive over warps
+        }
+        __syncthreads();
+        const long long excl = s_carry + (warp ? s_warp[warp - 1] : 0) + x - cnt;
+        if (i < N) chunk_first[i] = (int32_t)min64(excl, 0x7fffffffLL);
+        __syncthreads();
+        if (tid == 0) s_carry += s_warp[kPrepThreads / 32 - 1];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const long long total = s_carry;
+        const int bad = s_bad || total > chunks_ub;
+        chunk_first[N] = (int32_t)min64(total, 0x7fffffffLL);
+        hdr->total_chunks = bad ? 0 : (int32_t)total;
+        hdr->status = bad ? KDA_ERR_BAD_SEQLENS : KDA_OK;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout
+// ---------------------------------------------------------------------------
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+    int path;              // which prefill path runs
+    int64_t chunks_ub;     // upper bound on total chunks: ceil(T/C) + N
+    size_t table_off;      // int32 chunk_first[N+1]
+    size_t rec_off;        // per-(chunk, head) records
+    size_t rec_bytes;
+    size_t total;
+};
+
+static Layout layout_for(const kda_desc* d) {
+    Layout L;
+    L.path = choose_prefill_path(d->dtype, d->d_k);
+    L.chunks_ub = (d->total_tokens + kChunk - 1) / kChunk + d->num_seqs;
+    L.table_off = sizeof(DeviceHeader);
+    L.rec_off = align_up(L.table_off + ((size_t)d->num_seqs + 1) * sizeof(int32_t), 1024);
+    L.rec_bytes = prefill_record_bytes(L.path, d->d_k);
+    L.total = L.rec_off + (size_t)L.chunks_ub * d->num_heads * L.rec_bytes;
+    return L;
+}
+
+static bool desc_ok(const kda_desc* d) {
+    if (!d) return false;
+    if (d->num_seqs < 0 || d->num_heads < 1 || d->total_tokens < 0 || d->flags != 0) return false;
+    if (d->total_tokens > 0x7fffffffLL) return false;   // cu_seqlens is int32
+    if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return false;
+    if (d->d_k < 1 || d->d_v < 1) return false;
+    return true;
+}
+
+static bool shape_supported(const kda_desc* d) {
+    return d->d_k == d->d_v && (d->d_k == 64 || d->d_k == 128);
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+int kda_version(void) { return 10000; }
+
+int kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* kda_status_string(int s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_BAD_SEQLENS: return "KDA_ERR_BAD_SEQLENS";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+size_t kda_prefill_workspace_bytes(const kda_desc* d) {
+    if (!desc_ok(d) || !shape_supported(d)) return 0;
+    return layout_for(d).total;
+}
+
+int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
+                const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
+                const float* initial_state, void* out, float* final_state, kda_stream_t stream) {
+    if (!desc_ok(d)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!shape_supported(d)) return KDA_ERR_UNSUPPORTED;
+    const int N = d->num_seqs, H = d->num_heads, D = d->d_k;
+    const int64_t T = d->total_tokens;
+    if (cu_seqlens == nullptr && N != 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (N == 0) return KDA_OK;
+    const size_t esz = d->dtype == KDA_BF16 ? 2 : 4;
+    const size_t nqk = (size_t)T * H * D * esz, nb = (size_t)T * H * esz;
+    const size_t nstate = (size_t)N * H * D * D * sizeof(float);
+    if (T > 0) {
+        if (!q || !k || !v || !log_alpha || !beta || !out) return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+            ((uintptr_t)beta % esz) || !aligned16(out)) return KDA_ERR_INVALID_ARGUMENT;
+        const void* ins[5] = {q, k, v, log_alpha, beta};
+        const size_t szs[5] = {nqk, nqk, nqk, nqk, nb};
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(out, nqk, ins[i], szs[i])) return KDA_ERR_INVALID_ARGUMENT;
+        if (overlaps(out, nqk, initial_state, nstate) || overlaps(out, nqk, final_state, nstate))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if ((cu_seqlens && !aligned16(cu_seqlens)) || (initial_state && !aligned16(initial_state)) ||
+        (final_state && !aligned16(final_state))) return KDA_ERR_INVALID_ARGUMENT;
+    if (initial_state && final_state && initial_state != (const float*)final_state &&
+        overlaps(initial_state, nstate, final_state, nstate)) return KDA_ERR_INVALID_ARGUMENT;
+    const Layout L = layout_for(d);
+    if (!d->workspace || d->workspace_bytes < L.total || ((uintptr_t)d->workspace & 255u))
+        return KDA_ERR_WORKSPACE;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = (char*)d->workspace;
+    DeviceHeader* hdr = (DeviceHeader*)ws;
+    int32_t* chunk_first = (int32_t*)(ws + L.table_off);
+    kda_sequence_table<<<1, kPrepThreads, 0, s>>>(cu_seqlens, N, T, hdr, chunk_first, L.chunks_ub);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    PrefillArgs a;
+    a.dtype = d->dtype; a.d = D; a.N = N; a.H = H; a.chunks_ub = (int)L.chunks_ub;
+    a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.beta = beta;
+    a.cu = cu_seqlens ? cu_seqlens : hdr->pad;
+    a.s0 = initial_state; a.out = out; a.sf = final_state;
+    a.hdr = hdr; a.chunk_first = chunk_first; a.recs = ws + L.rec_off;
+    a.phase_events = (cudaEvent_t*)d->phase_events;
+    e = prefill_launch(L.path, a, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return KDA_OK;
+}
+
+int kda_decode_step(const kda_desc* d, const void* q, const void* k, const void* v,
+                    const void* log_alpha, const void* beta, float* state_inout, void* out,
+                    kda_stream_t stream) {
+    if (!desc_ok(d)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!shape_supported(d)) return KDA_ERR_UNSUPPORTED;
+    const int N = d->num_seqs, H = d->num_heads, D = d->d_k;
+    if (d->total_tokens != N) return KDA_ERR_INVALID_ARGUMENT;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !state_inout || !out) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t esz = d->dtype == KDA_BF16 ? 2 : 4;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || ((uintptr_t)beta % esz) ||
+        ((uintptr_t)state_inout & 31u) || !aligned16(out)) return KDA_ERR_INVALID_ARGUMENT;
+    if ((int64_t)N * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t nio = (size_t)N * H * D * esz, nstate = (size_t)N * H * D * D * sizeof(float);
+    const void* ins[5] = {q, k, v, log_alpha, beta};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(out, nio, ins[i], i == 4 ? (size_t)N * H * esz : nio) ||
+            overlaps(state_inout, nstate, ins[i], i == 4 ? (size_t)N * H * esz : nio))
+            return KDA_ERR_INVALID_ARGUMENT;
+    if (overlaps(out, nio, state_inout, nstate)) return KDA_ERR_INVALID_ARGUMENT;
+    cudaError_t e = decode_step_launch(d->dtype, D, q, k, v, log_alpha, beta, state_inout, out, N, H,
+                                       (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return KDA_OK;
+}
+
+int kda_get_device_status(const kda_desc* d, kda_stream_t stream) {
+    if (!d || !d->workspace || d->workspace_bytes < sizeof(DeviceHeader)) return KDA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t status = 0;
+    cudaError_t e = cudaMemcpyAsync(&status, d->workspace, sizeof(status), cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return status;
+}
+
+}  // extern "C"
+
+namespace kda {
+
+int choose_prefill_path(int dtype, int d) {
+    (void)dtype; (void)d;
+    return kPathSimt;
+}
+
+size_t prefill_record_bytes(int path, int d) {
+    (void)path;
+    return simt_record_bytes(d);
+}
+
+cudaError_t prefill_launch(int path, const PrefillArgs& a, cudaStream_t stream) {
+    (void)path;
+    return prefill_simt_launch(a, stream);
+}
+
+}  // namespace kda

@@ -1,0 +1,167 @@
+// kda_decode.cu -- kernel (c): one recurrent KDA decode step, state updated in place.
+//
+// Per (sequence, head) the step is ("Kimi Delta Attention" deep dive, section 06,
+// fused recurrent KDA; recurrence of section 03, read of section 02):
+//
+//     S' = Diag(alpha) S            alpha = exp(log_alpha)      [d_k x d_v]
+//     p  = S'^T k                   (what the decayed memory predicts at k)
+//     u  = beta (v - p)
+//     S  <- S' + k u^T              written back in place
+//     o  = S^T q = S'^T q + (k.q) u
+//
+// Both column reductions p and S'^T q come out of ONE pass over S, so the state
+// is read once and written once: the step is bound by HBM bandwidth on the
+// 2 * d_k * d_v * 4 bytes of fp32 state per (sequence, head).
+//
+// Grid: (N*H, d_v / 32).  A CTA owns a d_k x 32 column tile of one state
+// (columns of S are independent).  256 threads: 4 threads cover the 32 columns
+// of a row with 32-byte vectors (the widest global access on sm_100+), 64 rows
+// per pass, d_k/64 passes held in registers between the reduction and the
+// update.  State loads are issued before the small q/k/alpha staging so their
+// latency overlaps it; loads and stores carry an evict-first L2 hint because
+// the state is touched exactly once per step.
+#include "kda_common.cuh"
+#include "kda_paths.h"
+
+namespace kda {
+
+constexpr int kDecTile = 32;     // state columns per CTA
+constexpr int kDecThreads = 256;
+
+struct f8 { float v[8]; };
+
+__device__ __forceinline__ f8 ld_stream_f8(const float* p) {
+    uint32_t r[8];
+    asm volatile("ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]),
+                   "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]) : "l"(p));
+    f8 o;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o.v[i] = __uint_as_float(r[i]);
+    return o;
+}
+__device__ __forceinline__ void st_stream_f8(float* p, const f8& x) {
+    asm volatile("st.global.L1::no_allocate.L2::evict_first.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(__float_as_uint(x.v[0])), "r"(__float_as_uint(x.v[1])),
+                    "r"(__float_as_uint(x.v[2])), "r"(__float_as_uint(x.v[3])),
+                    "r"(__float_as_uint(x.v[4])), "r"(__float_as_uint(x.v[5])),
+                    "r"(__float_as_uint(x.v[6])), "r"(__float_as_uint(x.v[7])) : "memory");
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecThreads)
+kda_decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                       const T* __restrict__ log_alpha, const T* __restrict__ beta,
+                       float* __restrict__ state, T* __restrict__ out, int H) {
+    constexpr int kRowsPerPass = kDecThreads / 4;   // 64
+    constexpr int kPasses = D / kRowsPerPass;       // rows per thread
+    const int nh = blockIdx.x;                      // (sequence, head) pair, = n * H + h
+    const int col0 = blockIdx.y * kDecTile;
+    const int tid = threadIdx.x;
+    const int rsub = tid >> 2;                      // row within a pass
+    const int c8 = tid & 3;                         // which 8-float group of the tile
+
+    float* S = state + (size_t)nh * D * D;
+    f8 s[kPasses];
+#pragma unroll
+    for (int p = 0; p < kPasses; ++p)
+        s[p] = ld_stream_f8(S + (size_t)(p * kRowsPerPass + rsub) * D + col0 + c8 * 8);
+
+    __shared__ float sh_alpha[D], sh_k[D], sh_q[D];
+    __shared__ float sh_red[kDecThreads / 32][2][kDecTile];
+    __shared__ __align__(16) float sh_u[kDecTile];
+    __shared__ float sh_kq;
+
+    const size_t vec = (size_t)nh * D;              // q, k, log_alpha, v rows of this (n, h)
+    if (tid < D) {
+        sh_alpha[tid] = expf(to_f32(log_alpha[vec + tid]));
+        sh_k[tid] = to_f32(k[vec + tid]);
+        sh_q[tid] = to_f32(q[vec + tid]);
+    }
+    __syncthreads();
+    if (tid < 32) {                                 // k . q over the full key dimension
+        float a = 0.f;
+        for (int i = tid; i < D; i += 32) a += sh_k[i] * sh_q[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (tid == 0) sh_kq = a;
+    }
+
+    // Partial column sums of S'^T k and S'^T q over this thread's rows.
+    float pk[8], pq[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { pk[j] = 0.f; pq[j] = 0.f; }
+#pragma unroll
+    for (int p = 0; p < kPasses; ++p) {
+        const int r = p * kRowsPerPass + rsub;
+        const float a = sh_alpha[r], kr = sh_k[r], qr = sh_q[r];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            s[p].v[j] *= a;                         // S' = Diag(alpha) S
+            pk[j] += kr * s[p].v[j];
+            pq[j] += qr * s[p].v[j];
+        }
+    }
+    // Reduce over the 8 row groups of a warp (lanes differing in bits 2..4).
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            pk[j] += __shfl_xor_sync(0xffffffffu, pk[j], o);
+            pq[j] += __shfl_xor_sync(0xffffffffu, pq[j], o);
+        }
+    }
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane < 4) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            sh_red[warp][0][lane * 8 + j] = pk[j];
+            sh_red[warp][1][lane * 8 + j] = pq[j];
+        }
+    }
+    __syncthreads();
+    if (tid < kDecTile) {
+        float p = 0.f, r = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecThreads / 32; ++w) { p += sh_red[w][0][tid]; r += sh_red[w][1][tid]; }
+        const int j = col0 + tid;
+        const float b = to_f32(beta[nh]);
+        const float u = b * (to_f32(v[vec + j]) - p);   // u = beta (v - S'^T k)
+        sh_u[tid] = u;
+        out[vec + j] = from_f32<T>(r + sh_kq * u);      // o = S'^T q + (k.q) u
+    }
+    __syncthreads();
+    float u[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) u[j] = sh_u[c8 * 8 + j];
+#pragma unroll
+    for (int p = 0; p < kPasses; ++p) {
+        const int r = p * kRowsPerPass + rsub;
+        const float kr = sh_k[r];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[p].v[j] += kr * u[j];   // S' + k u^T
+        st_stream_f8(S + (size_t)r * D + col0 + c8 * 8, s[p]);
+    }
+}
+
+template <typename T, int D>
+static cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* la,
+                                 const void* beta, float* state, void* out, int N, int H,
+                                 cudaStream_t stream) {
+    dim3 grid((unsigned)N * H, D / kDecTile);
+    kda_decode_step_kernel<T, D><<<grid, kDecThreads, 0, stream>>>(
+        (const T*)q, (const T*)k, (const T*)v, (const T*)la, (const T*)beta, state, (T*)out, H);
+    return cudaGetLastError();
+}
+
+cudaError_t decode_step_launch(int dtype, int d, const void* q, const void* k, const void* v,
+                               const void* la, const void* beta, float* state, void* out,
+                               int N, int H, cudaStream_t stream) {
+    if (dtype == KDA_BF16)
+        return d == 128 ? launch_decode<__nv_bfloat16, 128>(q, k, v, la, beta, state, out, N, H, stream)
+                        : launch_decode<__nv_bfloat16, 64>(q, k, v, la, beta, state, out, N, H, stream);
+    return d == 128 ? launch_decode<float, 128>(q, k, v, la, beta, state, out, N, H, stream)
+                    : launch_decode<float, 64>(q, k, v, la, beta, state, out, N, H, stream);
+}
+
+}  // namespace kda

@@ -1,0 +1,41 @@
+// kda_paths.h -- host-side entry points of the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+enum PrefillPath { kPathSimt = 0, kPathTensorCore = 1 };
+
+// Which prefill implementation runs for a dtype and head size.
+int choose_prefill_path(int dtype, int d);
+// Bytes of workspace per (chunk, head) record for a path.
+size_t prefill_record_bytes(int path, int d);
+
+// Launch arguments shared by the prefill paths.
+struct PrefillArgs {
+    int dtype, d, N, H, chunks_ub;
+    const void *q, *k, *v, *la, *beta;
+    const int32_t* cu;           // device cu_seqlens (or the workspace copy)
+    const float* s0;             // initial state or nullptr
+    void* out;
+    float* sf;                   // final state or nullptr
+    void* hdr;                   // DeviceHeader in the workspace
+    const int32_t* chunk_first;  // [N+1] chunk offsets in the workspace
+    void* recs;                  // per-(chunk, head) records
+    cudaEvent_t* phase_events;   // optional timing events (3) or nullptr
+};
+
+cudaError_t prefill_launch(int path, const PrefillArgs& a, cudaStream_t stream);
+
+cudaError_t decode_step_launch(int dtype, int d, const void* q, const void* k, const void* v,
+                               const void* la, const void* beta, float* state, void* out,
+                               int N, int H, cudaStream_t stream);
+
+// CUDA-core (fp32) prefill.
+size_t simt_record_bytes(int d);
+cudaError_t prefill_simt_launch(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,189 @@
+"""Prefill on the GPU (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import assert_parity, host, rel_l2, to_device
+from synthetic import custom, prefill_inputs, workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import kda_gated_delta_chunked_gb300 as m
+    return m
+
+
+def run_gpu(kda, d, *, final=True, initial=True, stream=None):
+    g = to_device(d)
+    out, sf, ws = kda.prefill(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["cu_seqlens"],
+                              g["initial_state"] if initial else None, want_final_state=final,
+                              stream=stream)
+    torch.cuda.synchronize()
+    return out, sf, ws, g
+
+
+def run_oracle(d, initial=True, cols=None):
+    return oracle.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                          d["initial_state"] if initial else None, cols=cols)
+
+
+def test_workload0_single_f32_d64(kda):
+    w = workload(0)
+    d = prefill_inputs(w)
+    out, sf, _, _ = run_gpu(kda, d)
+    ro, rs = run_oracle(d)
+    assert_parity("workload0", host(out), ro, host(sf), rs, "f32")
+
+
+def test_workload1_single_bf16_T4096(kda):
+    w = workload(1)
+    d = prefill_inputs(w)
+    out, sf, _, _ = run_gpu(kda, d)
+    ro, rs = run_oracle(d)
+    assert_parity("workload1", host(out), ro, host(sf), rs, "bf16")
+
+
+@pytest.mark.parametrize("dtype,dim", [("bf16", 128), ("bf16", 64), ("f32", 128), ("f32", 64)])
+def test_ragged_varlen(kda, dtype, dim):
+    """Lengths around chunk boundaries, empty and 1-token sequences, several heads."""
+    lens = [0, 1, 2, 63, 64, 65, 0, 127, 129, 200]
+    w = custom(31 + dim, lens, 3, dim, dtype)
+    d = prefill_inputs(w)
+    out, sf, _, _ = run_gpu(kda, d)
+    ro, rs = run_oracle(d)
+    assert_parity(f"ragged {dtype} d{dim}", host(out), ro, host(sf), rs, dtype)
+    # an empty sequence hands its initial state straight through
+    s0 = d["initial_state"].double().numpy()
+    assert np.array_equal(host(sf)[0], s0[0]) and np.array_equal(host(sf)[6], s0[6])
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129])
+def test_single_sequence_lengths(kda, T):
+    w = custom(100 + T, [T], 2, 128, "bf16")
+    d = prefill_inputs(w)
+    out, sf, _, _ = run_gpu(kda, d)
+    ro, rs = run_oracle(d)
+    assert_parity(f"T={T}", host(out), ro, host(sf), rs, "bf16")
+
+
+def test_null_initial_and_final_state(kda):
+    w = custom(7, [130, 64], 2, 128, "bf16")
+    d = prefill_inputs(w)
+    out, sf, _, _ = run_gpu(kda, d, initial=False)
+    ro, rs = run_oracle(d, initial=False)
+    assert_parity("zero initial state", host(out), ro, host(sf), rs, "bf16")
+    out2, sf2, _, _ = run_gpu(kda, d, initial=False, final=False)
+    assert sf2 is None
+    assert torch.equal(out2, out)
+
+
+def test_final_state_aliases_initial_state(kda):
+    """In-place continuation: final_state == initial_state pointer."""
+    w = custom(8, [100, 37, 256], 2, 128, "bf16")
+    d = prefill_inputs(w)
+    g = to_device(d)
+    st = g["initial_state"].clone()
+    out, sf, _ = kda.prefill(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["cu_seqlens"],
+                             st, final_state=st)
+    torch.cuda.synchronize()
+    ro, rs = run_oracle(d)
+    assert_parity("aliased state", host(out), ro, host(st), rs, "bf16")
+
+
+def test_continuation_matches_single_call(kda):
+    """Prefix then suffix from the returned state equals one call (checkpoint semantics)."""
+    w = custom(9, [640], 2, 128, "bf16")
+    d = prefill_inputs(w)
+    g = to_device(d)
+    args = lambda a, b: [g[n][a:b] for n in ("q", "k", "v", "log_alpha", "beta")]
+    full, sfull, _ = kda.prefill(*args(0, 640), None, g["initial_state"])
+    for m in (64, 100, 333):
+        o1, s1, _ = kda.prefill(*args(0, m), None, g["initial_state"])
+        o2, s2, _ = kda.prefill(*args(m, 640), None, s1)
+        torch.cuda.synchronize()
+        assert rel_l2(host(torch.cat([o1, o2])), host(full)) < 5e-3
+        assert rel_l2(host(s2), host(sfull)) < 5e-3
+
+
+def test_varlen_isolation_on_gpu(kda):
+    """A packed batch equals each sequence run alone (bitwise: chunks restart per sequence)."""
+    lens = [77, 0, 150, 64]
+    w = custom(12, lens, 2, 128, "bf16")
+    d = prefill_inputs(w)
+    g = to_device(d)
+    out, sf, _ = kda.prefill(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["cu_seqlens"],
+                             g["initial_state"])
+    cu = d["cu_seqlens"].tolist()
+    for n in range(len(lens)):
+        a, b = cu[n], cu[n + 1]
+        if a == b:
+            continue
+        o1, s1, _ = kda.prefill(*(g[x][a:b] for x in ("q", "k", "v", "log_alpha", "beta")), None,
+                                g["initial_state"][n:n + 1].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(o1, out[a:b]) and torch.equal(s1[0], sf[n])
+
+
+def test_deterministic(kda):
+    w = custom(13, [300, 200], 4, 128, "bf16")
+    d = prefill_inputs(w)
+    o1, s1, _, _ = run_gpu(kda, d)
+    o2, s2, _, _ = run_gpu(kda, d)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+def test_bad_cu_seqlens_sets_device_status(kda):
+    w = custom(14, [64, 64], 2, 128, "bf16")
+    d = prefill_inputs(w)
+    g = to_device(d)
+    for bad in ([0, 100, 64], [5, 64, 128], [0, 64, 127]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        out, sf, ws = kda.prefill(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], cu, g["initial_state"])
+        desc = kda.make_desc(2, 2, 128, 128, 128, torch.bfloat16, ws)
+        assert kda.kda_get_device_status(desc) == kda.KDA_ERR_BAD_SEQLENS
+    out, sf, ws = kda.prefill(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["cu_seqlens"],
+                              g["initial_state"])
+    desc = kda.make_desc(2, 2, 128, 128, 128, torch.bfloat16, ws)
+    assert kda.kda_get_device_status(desc) == kda.KDA_OK
+
+
+def test_strong_decay_stress(kda):
+    """log alpha ~ -U(0.5, 5): per-chunk cumulative decays far beyond fp32 range
+    if formed naively; the result must stay finite and match the oracle."""
+    for dtype in ("bf16", "f32"):
+        w = custom(15, [200, 64], 2, 128, dtype, la_lo=0.5, la_hi=5.0)
+        d = prefill_inputs(w)
+        out, sf, _, _ = run_gpu(kda, d)
+        ro, rs = run_oracle(d)
+        assert_parity(f"strong decay {dtype}", host(out), ro, host(sf), rs, dtype)
+
+
+def test_workload2_varlen_full_size_sampled_columns(kda):
+    """The full 8-sequence varlen workload; the oracle computes 8 state columns exactly."""
+    w = workload(2)
+    d = prefill_inputs(w)
+    out, sf, _, _ = run_gpu(kda, d)
+    ro, rs = run_oracle(d, cols=(40, 48))
+    assert_parity("workload2 cols 40:48", host(out)[..., 40:48], ro[..., 40:48],
+                  host(sf)[..., 40:48], rs[..., 40:48], "bf16")
+
+
+def test_workload4_long_full_size_sampled(kda):
+    """The 1M-token workload as benchmarked; the oracle checks heads 0 and 9, 8 columns."""
+    w = workload(4)
+    d = prefill_inputs(w, device="cuda")
+    out, sf, _ = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                             d["initial_state"])
+    torch.cuda.synchronize()
+    heads = [0, 9]
+    sub = {n: d[n][:, heads].contiguous().cpu() for n in ("q", "k", "v", "log_alpha", "beta")}
+    ro, rs = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["log_alpha"], sub["beta"], None,
+                            d["initial_state"][:, heads].contiguous().cpu(), cols=(72, 80))
+    go = host(out[:, heads, 72:80])
+    gs = host(sf[:, heads, :, 72:80])
+    assert_parity("workload4 heads 0,9 cols 72:80", go, ro[..., 72:80], gs, rs[..., 72:80], "bf16")
