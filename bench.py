@@ -191,6 +191,7 @@ def run_ours(args, dist: Dist):
     w = workload(args.workload)
     T, H, D = w.total_tokens, w.num_heads, w.d_k
 
+    files = kda.prefill_kernel_files(w.dtype, D)
     # --- inputs resident in HBM (generated on the device by the seeded generator)
     x = prefill_inputs(w, device=dev)
     s0 = x["initial_state"]
@@ -252,18 +253,17 @@ def run_ours(args, dist: Dist):
     units = T * H
     state_bytes = 2 * H * D * D * 4
     tc_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    from kda_gated_delta_chunked_gb300 import _binding
     kinfo = {
         "intra": {"kernel": "kda intra-chunk (a)", "ms": intra_ms, "bound": "hbm",
                   "achieved": units * in_b / (intra_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                   "unit": "GB/s", "algorithmic_per_launch": units * in_b,
                   "tflops": units * intra_f / (intra_ms * 1e-3) / 1e12,
-                  "files": _binding.prefill_kernel_files(w.dtype, D)["intra"]},
+                  "files": files["intra"]},
         "chain": {"kernel": "kda inter-chunk (b)", "ms": chain_ms, "bound": "tensor",
                   "achieved": units * chain_f / (chain_ms * 1e-3) / 1e12, "peak": tc_peak,
                   "unit": "TFLOP/s", "algorithmic_per_launch": units * chain_f,
                   "gbs": (units * out_b + state_bytes) / (chain_ms * 1e-3) / 1e9,
-                  "files": _binding.prefill_kernel_files(w.dtype, D)["chain"]},
+                  "files": files["chain"]},
     }
     dom = max(kinfo, key=lambda k: kinfo[k]["ms"])
     kd = kinfo[dom]

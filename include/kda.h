@@ -73,6 +73,13 @@ typedef enum {
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
+/* kda_desc.flags bits. */
+enum {
+    /* Run the prefill on CUDA cores in fp32 even where the tensor-core path
+       applies (bf16, head size 128).  Slower; meant for cross-checking. */
+    KDA_FLAG_CUDA_CORE_PREFILL = 1
+};
+
 /* Problem description.  Not retained by the library after a call returns. */
 typedef struct kda_desc {
     int32_t num_seqs;       /* N >= 0 sequences (decode: sequences advanced by one token) */
@@ -81,7 +88,7 @@ typedef struct kda_desc {
     int32_t d_v;            /* value head size: must equal d_k */
     int64_t total_tokens;   /* T_tot = cu_seqlens[N] (decode: must equal N) */
     int32_t dtype;          /* kda_dtype of q, k, v, log_alpha, beta, out */
-    int32_t flags;          /* reserved, must be 0 */
+    int32_t flags;          /* 0 or KDA_FLAG_CUDA_CORE_PREFILL */
     void *workspace;        /* device scratch owned by the caller (prefill only), 256-byte aligned */
     size_t workspace_bytes; /* its size in bytes */
     void **phase_events;    /* optional timing hook (NULL: none): kda_prefill records

@@ -13,6 +13,7 @@ _LIB_PATH = os.environ.get("KDA_LIBRARY", os.path.join(_HERE, "_build", "libkda.
 KDA_OK, KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA = 0, 1, 2, 3
 KDA_ERR_TIMEOUT, KDA_ERR_BAD_SEQLENS, KDA_ERR_WORKSPACE = 4, 5, 6
 KDA_F32, KDA_BF16 = 0, 1
+KDA_FLAG_CUDA_CORE_PREFILL = 1
 
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_get_device_status",
            "kda_status_string", "kda_last_cuda_error", "kda_version")
@@ -62,9 +63,13 @@ def _load():
 lib = _load()
 
 
-def prefill_kernel_files(dtype: str, d: int):
+def prefill_kernel_files(dtype: str, d: int, flags: int = 0):
     """Source files of the two prefill kernels the library runs for a dtype and head size."""
-    return {"intra": ["kda_prefill_simt.cu"], "chain": ["kda_prefill_simt.cu"]}
+    if dtype == "bf16" and d == 128 and not (flags & KDA_FLAG_CUDA_CORE_PREFILL):
+        files = ["kda_prefill_tc.cu", "kda_sm100.cuh", "kda_common.cuh"]
+    else:
+        files = ["kda_prefill_simt.cu", "kda_common.cuh"]
+    return {"intra": files, "chain": files}
 
 
 def library_path() -> str:
@@ -88,9 +93,9 @@ _DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
 
 
 def make_desc(num_seqs: int, num_heads: int, d_k: int, d_v: int, total_tokens: int, dtype,
-              workspace: Optional[torch.Tensor] = None) -> KdaDesc:
+              workspace: Optional[torch.Tensor] = None, flags: int = 0) -> KdaDesc:
     dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
-    d = KdaDesc(num_seqs, num_heads, d_k, d_v, total_tokens, dt, 0, None, 0, None)
+    d = KdaDesc(num_seqs, num_heads, d_k, d_v, total_tokens, dt, flags, None, 0, None)
     if workspace is not None:
         d.workspace = workspace.data_ptr()
         d.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -133,7 +138,7 @@ def _check(t: torch.Tensor, name: str):
 
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, *, out=None,
-            final_state=None, workspace=None, stream=None, want_final_state: bool = True):
+            final_state=None, workspace=None, stream=None, want_final_state: bool = True, flags: int = 0):
     """Chunk-parallel prefill (see kda_prefill in include/kda.h).
 
     Allocates ``out``, ``final_state`` and the workspace with torch when they
@@ -147,7 +152,7 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, *, ou
         out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
     if final_state is None and want_final_state:
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-    desc = make_desc(N, H, dk, dv, T, q.dtype)
+    desc = make_desc(N, H, dk, dv, T, q.dtype, flags=flags)
     if workspace is None:
         nbytes = kda_prefill_workspace_bytes(desc)
         if nbytes == 0:

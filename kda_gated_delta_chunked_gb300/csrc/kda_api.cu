@@ -97,7 +97,7 @@ struct Layout {
 
 static Layout layout_for(const kda_desc* d) {
     Layout L;
-    L.path = choose_prefill_path(d->dtype, d->d_k);
+    L.path = choose_prefill_path(d->dtype, d->d_k, d->flags);
     L.chunks_ub = (d->total_tokens + kChunk - 1) / kChunk + d->num_seqs;
     L.table_off = sizeof(DeviceHeader);
     L.rec_off = align_up(L.table_off + ((size_t)d->num_seqs + 1) * sizeof(int32_t), 1024);
@@ -108,7 +108,8 @@ static Layout layout_for(const kda_desc* d) {
 
 static bool desc_ok(const kda_desc* d) {
     if (!d) return false;
-    if (d->num_seqs < 0 || d->num_heads < 1 || d->total_tokens < 0 || d->flags != 0) return false;
+    if (d->num_seqs < 0 || d->num_heads < 1 || d->total_tokens < 0) return false;
+    if (d->flags & ~KDA_FLAG_CUDA_CORE_PREFILL) return false;
     if (d->total_tokens > 0x7fffffffLL) return false;   // cu_seqlens is int32
     if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return false;
     if (d->d_k < 1 || d->d_v < 1) return false;
@@ -194,7 +195,7 @@ int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     PrefillArgs a;
-    a.dtype = d->dtype; a.d = D; a.N = N; a.H = H; a.chunks_ub = (int)L.chunks_ub;
+    a.dtype = d->dtype; a.d = D; a.N = N; a.H = H; a.chunks_ub = (int)L.chunks_ub; a.T = T;
     a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.beta = beta;
     a.cu = cu_seqlens ? cu_seqlens : hdr->pad;
     a.s0 = initial_state; a.out = out; a.sf = final_state;
@@ -246,18 +247,17 @@ int kda_get_device_status(const kda_desc* d, kda_stream_t stream) {
 
 namespace kda {
 
-int choose_prefill_path(int dtype, int d) {
-    (void)dtype; (void)d;
+int choose_prefill_path(int dtype, int d, int flags) {
+    if ((flags & KDA_FLAG_CUDA_CORE_PREFILL) == 0 && dtype == KDA_BF16 && d == 128) return kPathTensorCore;
     return kPathSimt;
 }
 
 size_t prefill_record_bytes(int path, int d) {
-    (void)path;
-    return simt_record_bytes(d);
+    return path == kPathTensorCore ? tc_record_bytes() : simt_record_bytes(d);
 }
 
 cudaError_t prefill_launch(int path, const PrefillArgs& a, cudaStream_t stream) {
-    (void)path;
+    if (path == kPathTensorCore) return prefill_tc_launch(a, a.T, stream);
     return prefill_simt_launch(a, stream);
 }
 

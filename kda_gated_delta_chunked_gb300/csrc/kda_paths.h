@@ -9,14 +9,15 @@ namespace kda {
 
 enum PrefillPath { kPathSimt = 0, kPathTensorCore = 1 };
 
-// Which prefill implementation runs for a dtype and head size.
-int choose_prefill_path(int dtype, int d);
+// Which prefill implementation runs for a dtype, head size and desc flags.
+int choose_prefill_path(int dtype, int d, int flags);
 // Bytes of workspace per (chunk, head) record for a path.
 size_t prefill_record_bytes(int path, int d);
 
 // Launch arguments shared by the prefill paths.
 struct PrefillArgs {
     int dtype, d, N, H, chunks_ub;
+    int64_t T;                   // total tokens
     const void *q, *k, *v, *la, *beta;
     const int32_t* cu;           // device cu_seqlens (or the workspace copy)
     const float* s0;             // initial state or nullptr
@@ -37,5 +38,9 @@ cudaError_t decode_step_launch(int dtype, int d, const void* q, const void* k, c
 // CUDA-core (fp32) prefill.
 size_t simt_record_bytes(int d);
 cudaError_t prefill_simt_launch(const PrefillArgs& a, cudaStream_t stream);
+
+// Tensor-core (tcgen05) prefill: bf16 inputs, head size 128.
+size_t tc_record_bytes();
+cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stream);
 
 }  // namespace kda

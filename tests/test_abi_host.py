@@ -72,7 +72,7 @@ def test_prefill_host_validation():
     bad = kda.make_desc(2, 4, 96, 96, 256, torch.bfloat16)
     assert kda.kda_prefill(bad, q, k, v, la, b, cu, s0, out, sf, 0) == kda.KDA_ERR_UNSUPPORTED
     # flags must be 0, dtype must be known
-    bad = kda.make_desc(2, 4, 128, 128, 256, torch.bfloat16); bad.flags = 1
+    bad = kda.make_desc(2, 4, 128, 128, 256, torch.bfloat16); bad.flags = 2
     assert kda.kda_prefill(bad, q, k, v, la, b, cu, s0, out, sf, 0) == kda.KDA_ERR_INVALID_ARGUMENT
     bad = kda.make_desc(2, 4, 128, 128, 256, 7)
     assert kda.kda_prefill(bad, q, k, v, la, b, cu, s0, out, sf, 0) == kda.KDA_ERR_INVALID_ARGUMENT
