@@ -154,6 +154,43 @@ KDA_API int kda_decode_step(const kda_desc *desc,
  */
 KDA_API int kda_get_device_status(const kda_desc *desc, kda_stream_t stream);
 
+/*
+ * Size of the fixed scratch area kda_prefill_noalloc uses: 64 MiB.
+ */
+#define KDA_PREFILL_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * kda_prefill without a workspace, for callers that cannot allocate device
+ * memory: code that gets all its buffers from someone else's pool, plugins
+ * given only their inputs and outputs, or code where a cudaMalloc would
+ * synchronise the device at the wrong moment.  The pages have no counterpart
+ * to this call; it is a convenience of this library.
+ *
+ * Same arguments, layouts and results as kda_prefill; desc->workspace and
+ * desc->workspace_bytes are ignored.  Instead the library's own static
+ * device array of KDA_PREFILL_NOALLOC_SCRATCH_BYTES is used.  The runtime
+ * reserves it on each device where this call is first used and holds it until
+ * the process exits; no call allocates or frees anything.
+ *  - Problems needing more scratch than that (kda_prefill_workspace_bytes
+ *    larger than KDA_PREFILL_NOALLOC_SCRATCH_BYTES, for example more than about
+ *    800 chunk-heads of 64 tokens on the bf16 head-size-128 path) are rejected
+ *    with KDA_ERR_WORKSPACE before any GPU work.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents (nothing in it needs to start at zero).  Calls whose GPU work
+ *    may overlap -- different streams, or host threads without ordering --
+ *    race on it and must be serialised by the caller.
+ *  - The device status word lives in that array too; kda_get_device_status
+ *    cannot read it.
+ */
+KDA_API int kda_prefill_noalloc(const kda_desc *desc,
+                                const void *q, const void *k, const void *v,
+                                const void *log_alpha, const void *beta,
+                                const int32_t *cu_seqlens, const float *initial_state,
+                                void *out, float *final_state, kda_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 KDA_API const char *kda_status_string(int status);
 

@@ -13,5 +13,6 @@ from ._binding import (  # noqa: F401
     KdaError, prefill_kernel_files,
     library_path, lib, exported_symbols,
     kda_prefill_workspace_bytes, kda_prefill, kda_decode_step, kda_get_device_status,
-    kda_status_string, kda_version, make_desc, prefill, decode_step,
+    kda_status_string, kda_version, make_desc, prefill, decode_step, kda_prefill_noalloc,
+    KDA_PREFILL_NOALLOC_SCRATCH_BYTES,
 )

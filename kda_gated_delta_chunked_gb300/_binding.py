@@ -16,7 +16,8 @@ KDA_F32, KDA_BF16 = 0, 1
 KDA_FLAG_CUDA_CORE_PREFILL = 1
 
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_get_device_status",
-           "kda_status_string", "kda_last_cuda_error", "kda_version")
+           "kda_status_string", "kda_last_cuda_error", "kda_version", "kda_prefill_noalloc")
+KDA_PREFILL_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class KdaDesc(ctypes.Structure):
@@ -47,6 +48,8 @@ def _load():
     L.kda_prefill_workspace_bytes.restype = ctypes.c_size_t
     L.kda_prefill.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kda_prefill.restype = ctypes.c_int
+    L.kda_prefill_noalloc.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.kda_prefill_noalloc.restype = ctypes.c_int
     L.kda_decode_step.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kda_decode_step.restype = ctypes.c_int
     L.kda_get_device_status.argtypes = [D, vp]
@@ -121,6 +124,13 @@ def kda_prefill(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, initial_sta
     """Raw C call: every tensor argument is passed as its data pointer (or NULL)."""
     return lib.kda_prefill(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
                            _p(cu_seqlens), _p(initial_state), _p(out), _p(final_state), _stream(stream))
+
+
+def kda_prefill_noalloc(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state,
+                        stream=None) -> int:
+    """Raw C call of the no-workspace prefill (the library's fixed scratch area)."""
+    return lib.kda_prefill_noalloc(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
+                                   _p(cu_seqlens), _p(initial_state), _p(out), _p(final_state), _stream(stream))
 
 
 def kda_decode_step(desc: KdaDesc, q, k, v, log_alpha, beta, state_inout, out, stream=None) -> int:
