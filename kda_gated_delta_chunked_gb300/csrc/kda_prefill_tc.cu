@@ -18,25 +18,34 @@
 // chunk, the recurrent state carried between chunks; the recurrence itself is
 // that of section 03.)
 //
-// Kernel (a), one CTA per (chunk, head), 128 threads:
-//   1. TMA loads the q, k, v, log_alpha tiles [64 tokens x 128].
-//   2. Thread c owns key channel c: running sum g, then every scaled operand
-//      (K~, Q~, K^ around a mid-chunk reference for the Gram products; K~ and
-//      Q~ from the chunk start and V, transposed, for the second product;
-//      K^end transposed for kernel b), written as bf16 in the 128-byte-swizzle
-//      K-major layout the tensor core reads.
-//   3. MMA-a (M=128, N=64, K=128): [K~m; Q~m] K^m^T gives the Gram block (rows
-//      0..63, -> A) and the P block (rows 64..127) in one TMEM accumulator.
-//   4. One recursion per row gives [T; P T] at once: Y (I + A) = [I; P], solved
-//      column by column from the right, then scaled by Diag(beta).
-//   5. MMA-b (M=128, N=256 then 128, K=64+64):
-//        [[T, 0], [P T, -I]] x [[K~, V], [Q~, 0]] = [[W, U0], [-Q', O0]].
-//   6. The records kernel (b) reads are written as ready-to-copy shared-memory
-//      images: [W; Q'] and K^end^T in the swizzled K-major layout, U0 / O0 in
-//      16-column tiles, Gamma.
+// Kernel (a), one CTA per (chunk, head), 256 threads, two CTAs per SM:
+//   1. Each thread owns 4 token rows x 8 key channels of the chunk: 16-byte
+//      loads of k, q, log_alpha, a running sum of log alpha within its rows
+//      and a prefix over the 16 row groups through shared memory.  It then
+//      writes every scaled operand as bf16 with 16-byte stores, all
+//      token-major (no transposes): K~m, Q~m, K^m around a mid-chunk
+//      reference g_m, and K^end straight into the record.  V goes from HBM to
+//      the tensor core untouched (TMA, 128-byte swizzle).
+//   2. MMA-a (M=128, N=64, K=128): [K~m; Q~m] K^m^T gives the Gram block (rows
+//      0..63) and Q~ K^T (rows 64..127) in one TMEM accumulator.
+//   3. With A^[i][j] = beta_j (K~ K^T)[i][j] (j < i), the rows of
+//      Y^ = [T; P T] solve  Y^ (I + A^) = [Diag(beta); P Diag(beta)]  (beta
+//      folded into the columns, so the solution needs no later rescaling).
+//      The solve runs in 16-column blocks from the right: the coupling to the
+//      already solved blocks is one small MMA (M=128, N=16) from the bf16 Y^
+//      and A^ (stored row by row, read MN-major), the 16 x 16 diagonal block a
+//      short fp32 recursion.
+//   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~m | V] with K~m read MN-major
+//      from the MMA-a operand; since K~ = K~m Diag(2^g_m), W, P T K~ and Q~
+//      are rescaled per channel in the epilogue, Q' = Q~ - P T K~.
+//   5. The records kernel (b) reads are written as ready-to-copy shared-memory
+//      images: [W; Q'] (K-major, 128-byte swizzle), K^end (token-major), U0 /
+//      O0 in 16-column tiles, Gamma.
 // Chunks whose cumulative decay spans more than 2^100 inside the chunk cannot
-// use the mid-reference factorisation in fp32; for those the Gram and P blocks
-// are formed on CUDA cores with exp(g_i - g_j) inside the sum (never > 1).
+// use the mid-reference factorisation in fp32; for those the Gram and Q~ K^T
+// rows are formed on CUDA cores with exp(g_i - g_j) (never > 1) inside the
+// channel sums and stored to TMEM where MMA-a would have put them, and the
+// reference point moves to the chunk start (g_m = 0).
 //
 // Kernel (b), one CTA per (sequence, head, 16-column tile of the state):
 // a producer warp streams each chunk's record into a 3-stage shared-memory
@@ -45,7 +54,7 @@
 //   MMA1 (M=128, N=16, K=128): [W; Q'] S  -> U = U0 - W S (rows 0..63),
 //                                             O = O0 + Q' S (rows 64..127)
 //   MMA3 (M=128, N=16, K=64):  K^end^T U  -> S <- Gamma * S + K^end^T U
-// with S and U fed back to the tensor core as bf16 operands.
+// with S and U fed back to the tensor core as bf16 MN-major operands.
 //
 // Every wait on an mbarrier is bounded; on timeout the kernel records
 // KDA_ERR_TIMEOUT in the device status word, drains its own copies and exits.
@@ -64,12 +73,12 @@ constexpr int kTile = 16;                // state columns per CTA of kernel (b)
 constexpr int kTiles = kTcD / kTile;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMaxSpanLog2 = 100.f;    // fast path if max_c (g_0 - g_C) <= 2^100 (log2 units)
+constexpr float kMaxSpanLog2 = 100.f;    // fast path if max_c (g_0 - g_C) <= 100 (log2 units)
 
 // Record of one (chunk, head), bytes.
 struct TcRec {
     static constexpr uint32_t kA1 = 0;          // [W; Q'] image: 2 K-blocks x [128 rows x 128 B]
-    static constexpr uint32_t kKE = 32768;      // K^end^T image: [128 rows x 128 B]
+    static constexpr uint32_t kKE = 32768;      // K^end image: token-major, 2 x [64 tok x 64 ch]
     static constexpr uint32_t kU0 = 49152;      // U0: 8 tiles x [64 tokens x 16] bf16
     static constexpr uint32_t kO0 = 65536;      // O0: same layout
     static constexpr uint32_t kGam = 81920;     // Gamma: 128 fp32
@@ -79,39 +88,130 @@ struct TcRec {
 
 size_t tc_record_bytes() { return TcRec::kBytes; }
 
-// ---------------------------------------------------------------------------
-// Kernel (a)
-// ---------------------------------------------------------------------------
-struct SmemA {   // byte offsets from a 1024-aligned base
-    static constexpr uint32_t kIn = 0;          // K, Q, LA, V tiles (TMA), 4 x 16 KB
-    static constexpr uint32_t kInK = 0, kInQ = 16384, kInLA = 32768, kInV = 49152;
-    static constexpr uint32_t kOpA = 65536;     // MMA-a A [K~m; Q~m], 32 KB; later At fp32 (16 KB)
-    static constexpr uint32_t kOpB1 = 98304;    // MMA-a B K^m, 16 KB
-    static constexpr uint32_t kOpB2 = 114688;   // MMA-b B: [K~^T; V^T] (32 KB) + Q~^T (16 KB)
-    static constexpr uint32_t kKE = 163840;     // K^end^T image, 16 KB
-    static constexpr uint32_t kMisc = 180224;   // beta, flags, barriers
-    static constexpr uint32_t kBytes = 181248 + 1024;
-    // After step 2: MMA-b A operand [[T,0],[PT,-I]] reuses the K/Q tiles (32 KB),
-    // the slow path keeps g (fp32 [64][128]) in the LA/V tiles.
-};
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&p);
 }
+__device__ __forceinline__ float bf_lo(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
 
-__global__ void __launch_bounds__(128, 1)
-kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
+// ---------------------------------------------------------------------------
+// Kernel (a)
+// ---------------------------------------------------------------------------
+constexpr int kAThreads = 256;
+
+struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per SM
+    static constexpr uint32_t kV = 0;           // V tile (TMA, 128-byte swizzle), 2 x [64 tok x 64 ch]
+    static constexpr uint32_t kOpA = 16384;     // [K~m; Q~m], K-major 128B-swizzle, 2 K-blocks x 16 KB;
+                                                // MMA-a A, then MMA-b B (MN-major) and Q~m for the epilogue
+    static constexpr uint32_t kOpB1 = 49152;    // MMA-a B K^m, K-major, 2 K-blocks x 8 KB; then:
+    static constexpr uint32_t kAt = 49152;      //   A^ by 16-column blocks, MN-major 32B-swizzle, 4 x 2 KB
+    static constexpr uint32_t kAt32 = 57344;    //   diagonal 16 x 16 blocks of A^ transposed, fp32, 4 KB
+    static constexpr uint32_t kY = 65536;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB
+    static constexpr uint32_t kPart = 65536;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
+    static constexpr uint32_t kGS = 49152;      // (slow path, before A^) g, fp32 [64][128], 32 KB
+    static constexpr uint32_t kMisc = 81920;    // beta[64], Em[128], barriers, TMEM slot, flags
+    static constexpr uint32_t kBytes = kMisc + 2048 + 1024;
+};
+
+// Byte offset of (row m, column n < 16) in a 16-column block of an MN-major
+// operand with 32-byte swizzle: 32-byte rows, 8-row groups of 256 bytes, the
+// two 16-byte halves of a row swapped on rows 4..7 of each group.
+__device__ __forceinline__ uint32_t sw32_off(uint32_t m, uint32_t n) {
+    return (m >> 3) * 256u + (m & 7u) * 32u + ((((n >> 3) ^ ((m & 7u) >> 2)) & 1u) << 4) + (n & 7u) * 2u;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+// Column block J (16 columns) of the solve Y^ (I + A^) = RHS for row `tid`
+// (threads 0..127) of Y^: the right-hand side (from the Gram / Q~ K^T
+// accumulator still in TMEM columns 0..63), minus the coupling to the solved
+// blocks on the right (one MMA from the bf16 Y^ and A^ into TMEM columns
+// 64..79), then the in-block recursion on the fp32 diagonal block; stored to
+// Y^ as bf16.  Threads 128..255 only take part in the barrier.
+template <int J>
+__device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const float* s_beta, uint64_t* bar,
+                                          int* s_flag, uint32_t& mph, bool& abort) {
+    const int tid = threadIdx.x, warp = tid >> 5;
+    uint8_t* yop = sm + SmemA::kY;
+    if (J < 3 && tid == 0 && !abort) {
+#pragma unroll
+        for (int ks = J + 1; ks < 4; ++ks)
+            mma_bf16_ss(tmem + 64, sdesc_k_sw128(smem_u32(yop + ks * 32)),
+                        sdesc(smem_u32(sm + SmemA::kAt + J * 2048 + ks * 512), 2048, 256, 6),
+                        idesc_bf16(128, 16, 0, 1), ks > J + 1);
+        mma_commit(bar);
+    }
+    if (warp < 4) {
+        const float4* at32v = (const float4*)(sm + SmemA::kAt32);
+        float z[16];
+        if (warp < 2) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) z[jj] = (16 * J + jj == tid) ? s_beta[tid] : 0.f;
+        } else {
+            const int i = tid - 64;
+            float f[16];
+            tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * J), f);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) z[jj] = (16 * J + jj <= i) ? f[jj] * s_beta[16 * J + jj] : 0.f;
+        }
+        if (J < 3) {
+            if (!abort && !mbar_wait(bar, mph & 1, kWaitNs)) s_flag[1] = 1;
+            tc_fence_after_sync();
+            float dd[16];
+            tmem_ld16(tmem_addr(tmem, 32 * warp, 64), dd);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) z[jj] -= dd[jj];
+        }
+#pragma unroll
+        for (int jj = 14; jj >= 0; --jj) {
+            float acc = z[jj];
+#pragma unroll
+            for (int g4 = (jj + 1) >> 2; g4 < 4; ++g4) {
+                const float4 a = at32v[(J * 16 + jj) * 4 + g4];
+                if (4 * g4 + 0 > jj) acc = fmaf(-z[4 * g4 + 0], a.x, acc);
+                if (4 * g4 + 1 > jj) acc = fmaf(-z[4 * g4 + 1], a.y, acc);
+                if (4 * g4 + 2 > jj) acc = fmaf(-z[4 * g4 + 2], a.z, acc);
+                if (4 * g4 + 3 > jj) acc = fmaf(-z[4 * g4 + 3], a.w, acc);
+            }
+            z[jj] = acc;
+        }
+        uint32_t p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p[e] = pack_bf16x2(z[2 * e], z[2 * e + 1]);
+        *(uint4*)(yop + sw128_off(tid, 16 * J)) = make_uint4(p[0], p[1], p[2], p[3]);
+        *(uint4*)(yop + sw128_off(tid, 16 * J + 8)) = make_uint4(p[4], p[5], p[6], p[7]);
+        fence_proxy_async_smem();
+    }
+    if (J < 3) ++mph;
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    abort = s_flag[1] != 0;
+}
+
+__global__ void __launch_bounds__(kAThreads, 2)
+kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ q,
+                   const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ log_alpha,
                    const __nv_bfloat16* __restrict__ beta, const int32_t* __restrict__ cu,
                    DeviceHeader* __restrict__ hdr, const int32_t* __restrict__ chunk_first, int N, int H,
                    uint8_t* __restrict__ recs) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* s_beta = (float*)(sm + SmemA::kMisc);                 // [64]
-    uint64_t* bars = (uint64_t*)(sm + SmemA::kMisc + 256);       // [0] inputs, [1] mma
-    uint32_t* s_tmem = (uint32_t*)(sm + SmemA::kMisc + 512);
-    int* s_flag = (int*)(sm + SmemA::kMisc + 528);                // [0] slow path, [1] abort
+    float* s_em = (float*)(sm + SmemA::kMisc + 256);             // [128] 2^(g_m) per channel
+    uint64_t* bars = (uint64_t*)(sm + SmemA::kMisc + 768);       // [0] V tile, [1] MMAs
+    uint32_t* s_tmem = (uint32_t*)(sm + SmemA::kMisc + 800);
+    int* s_flag = (int*)(sm + SmemA::kMisc + 816);                // [0] slow path, [1] abort
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (hdr->status != KDA_OK) return;
@@ -128,106 +228,135 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_mbar_init();
         s_flag[0] = 0;
         s_flag[1] = 0;
-        prefetch_tensormap(&tm_q); prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v); prefetch_tensormap(&tm_la);
     }
     __syncthreads();
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[0], 4 * 16384);
-        tma_load_3d(sm + SmemA::kInK, &tm_k, 0, h, (int)t0, &bars[0]);
-        tma_load_3d(sm + SmemA::kInQ, &tm_q, 0, h, (int)t0, &bars[0]);
-        tma_load_3d(sm + SmemA::kInLA, &tm_la, 0, h, (int)t0, &bars[0]);
-        tma_load_3d(sm + SmemA::kInV, &tm_v, 0, h, (int)t0, &bars[0]);
+        mbar_arrive_expect_tx(&bars[0], 16384);
+        tma_load_3d(sm + SmemA::kV, &tm_v, 0, h, (int)t0, &bars[0]);
+        tma_load_3d(sm + SmemA::kV + 8192, &tm_v, 64, h, (int)t0, &bars[0]);
     }
     if (tid < kChunk) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
     if (warp == 0) { tmem_alloc(s_tmem, 256); tmem_relinquish(); }
-    if (!mbar_wait(&bars[0], 0, kWaitNs)) s_flag[1] = 1;
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem = *s_tmem;
-    bool abort = s_flag[1] != 0;
 
-    // ---- step 2a: running sum of log alpha for channel c (log2 units) ----
-    const int ch = tid;                        // key channel owned by this thread
-    const __nv_bfloat16* inK = (const __nv_bfloat16*)(sm + SmemA::kInK);
-    const __nv_bfloat16* inQ = (const __nv_bfloat16*)(sm + SmemA::kInQ);
-    const __nv_bfloat16* inL = (const __nv_bfloat16*)(sm + SmemA::kInLA);
-    const __nv_bfloat16* inV = (const __nv_bfloat16*)(sm + SmemA::kInV);
-    float G[kChunk];
+    // ---- pass A: thread owns rows 4R..4R+3, channels 8C..8C+7.  16-byte loads,
+    // running sum of log alpha (log2 units) within the 4 rows.
+    const int R = tid >> 4, C = tid & 15;
+    const size_t rs = (size_t)H * kTcD;                       // elements between tokens
+    const size_t base = ((size_t)t0 * H + h) * kTcD + 8 * C;
+    float gl[4][8];
+    uint4 kr[4], qr[4];
     {
-        float g = 0.f;
+        float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int r = 0; r < kChunk; ++r) {
-            const float la = r < len ? __bfloat162float(inL[r * kTcD + ch]) : 0.f;
-            g = fmaf(la, kLog2e, g);
-            G[r] = g;
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * R + i;
+            const bool ok = r < len;
+            const size_t gi = base + (size_t)r * rs;
+            const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 la4 = ok ? *(const uint4*)(log_alpha + gi) : z4;
+            kr[i] = ok ? *(const uint4*)(k + gi) : z4;
+            qr[i] = ok ? *(const uint4*)(q + gi) : z4;
+            float la[8];
+            unpack8(la4, la);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { s8[e] = fmaf(la[e], kLog2e, s8[e]); gl[i][e] = s8[e]; }
+        }
+        float4* part = (float4*)(sm + SmemA::kPart) + (R * kTcD + 8 * C) / 4;
+        part[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
+        part[1] = make_float4(s8[4], s8[5], s8[6], s8[7]);
+    }
+    __syncthreads();
+    // Prefix over the 16 row groups: g before this thread's rows, at row 31 (g_m)
+    // and at row 63 (g_C), for its 8 channels.
+    float gbase[8], gm[8], gC[8];
+    {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const float4* part = (const float4*)(sm + SmemA::kPart);
+#pragma unroll 4
+        for (int rg = 0; rg < 16; ++rg) {
+            if (rg == R) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gbase[e] = acc[e];
+            }
+            if (rg == 8) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gm[e] = acc[e];
+            }
+            const float4 a = part[(rg * kTcD + 8 * C) / 4], b = part[(rg * kTcD + 8 * C) / 4 + 1];
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gC[e] = acc[e];
+        if (R == 0) {
+            bool wide = false;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wide |= (gl[0][e] - gC[e] > kMaxSpanLog2);
+            if (wide) s_flag[0] = 1;                    // any writer sets 1
         }
     }
-    const float gm = G[31], gC = G[kChunk - 1];
-    if (G[0] - gC > kMaxSpanLog2) s_flag[0] = 1;   // benign race: any writer sets 1
-    __syncthreads();
+    tc_fence_before_sync();
+    __syncthreads();                                    // also: kPart no longer read
+    tc_fence_after_sync();
+    const uint32_t tmem = *s_tmem;
     const bool slow = s_flag[0] != 0;
+    if (slow) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gm[e] = 0.f;      // reference at the chunk start: nothing exceeds 1
+    }
+    if (R == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            s_em[8 * C + e] = exp2f(gm[e]);
+            ((float*)(rec + TcRec::kGam))[8 * C + e] = exp2f(gC[e]);
+        }
+    }
 
-    // ---- step 2b: scaled operands ----
+    // ---- pass B: scaled operands for the thread's 4 rows x 8 channels.
     {
-        const uint32_t kb = (uint32_t)ch >> 6, kin = (uint32_t)ch & 63u;
+        const uint32_t kb = (uint32_t)C >> 3, cc = (uint32_t)(C & 7) * 8u;
         uint8_t* opA = sm + SmemA::kOpA + kb * 16384;
         uint8_t* opB1 = sm + SmemA::kOpB1 + kb * 8192;
-        uint8_t* opB2 = sm + SmemA::kOpB2;
-        uint8_t* keI = sm + SmemA::kKE;
-        const float Em = exp2f(gm), ECm = exp2f(gC - gm);
-        uint32_t kt[4], qt[4], vt[4], ke[4];
+        uint8_t* ke = rec + TcRec::kKE + kb * 8192;
+        float* gS = (float*)(sm + SmemA::kGS);
 #pragma unroll
-        for (int r = 0; r < kChunk; ++r) {
-            const bool ok = r < len;
-            const float kv = ok ? __bfloat162float(inK[r * kTcD + ch]) : 0.f;
-            const float qv = ok ? __bfloat162float(inQ[r * kTcD + ch]) : 0.f;
-            const float vv = ok ? __bfloat162float(inV[r * kTcD + ch]) : 0.f;
-            float e3, e4;
-            if (!slow) {
-                const float e1 = exp2f(G[r] - gm);         // 2^(g_r - g_m)
-                const float e2 = exp2f(gm - G[r]);         // 2^(g_m - g_r)
-                e3 = e1 * Em;                              // 2^(g_r)        <= 1
-                e4 = e2 * ECm;                             // 2^(g_C - g_r)  <= 1
-                *(__nv_bfloat16*)(opA + sw128_off(r, kin)) = __float2bfloat16_rn(kv * e1);
-                *(__nv_bfloat16*)(opA + sw128_off(64 + r, kin)) = __float2bfloat16_rn(qv * e1);
-                *(__nv_bfloat16*)(opB1 + sw128_off(r, kin)) = __float2bfloat16_rn(kv * e2);
-            } else {
-                e3 = exp2f(G[r]);
-                e4 = exp2f(gC - G[r]);
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * R + i;
+            float kv[8], qv[8], km[8], qm[8], kh[8], kend[8];
+            unpack8(kr[i], kv);
+            unpack8(qr[i], qv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float g = gbase[e] + gl[i][e];
+                if (!slow) {
+                    const float e1 = exp2f(g - gm[e]);        // 2^(g_r - g_m)
+                    const float e2 = exp2f(gm[e] - g);        // 2^(g_m - g_r)
+                    km[e] = kv[e] * e1;
+                    qm[e] = qv[e] * e1;
+                    kh[e] = kv[e] * e2;
+                    kend[e] = kh[e] * exp2f(gC[e] - gm[e]);  // k 2^(g_C - g_r) <= |k|
+                } else {
+                    const float e3 = exp2f(g);
+                    km[e] = kv[e] * e3;
+                    qm[e] = qv[e] * e3;
+                    kend[e] = kv[e] * exp2f(gC[e] - g);
+                    gS[r * kTcD + 8 * C + e] = g;
+                }
             }
-            const int w = (r & 7) >> 1;
-            if ((r & 1) == 0) {
-                kt[w] = pack_bf16x2(kv * e3, 0.f); qt[w] = pack_bf16x2(qv * e3, 0.f);
-                vt[w] = pack_bf16x2(vv, 0.f);      ke[w] = pack_bf16x2(kv * e4, 0.f);
-            } else {
-                kt[w] = (kt[w] & 0xffffu) | (pack_bf16x2(0.f, kv * e3) & 0xffff0000u);
-                qt[w] = (qt[w] & 0xffffu) | (pack_bf16x2(0.f, qv * e3) & 0xffff0000u);
-                vt[w] = (vt[w] & 0xffffu) | (pack_bf16x2(0.f, vv) & 0xffff0000u);
-                ke[w] = (ke[w] & 0xffffu) | (pack_bf16x2(0.f, kv * e4) & 0xffff0000u);
-            }
-            if ((r & 7) == 7) {
-                const uint32_t r8 = (uint32_t)(r & ~7);
-                *(uint4*)(opB2 + sw128_off(ch, r8)) = make_uint4(kt[0], kt[1], kt[2], kt[3]);
-                *(uint4*)(opB2 + sw128_off(128 + ch, r8)) = make_uint4(vt[0], vt[1], vt[2], vt[3]);
-                *(uint4*)(opB2 + 32768 + sw128_off(ch, r8)) = make_uint4(qt[0], qt[1], qt[2], qt[3]);
-                *(uint4*)(keI + sw128_off(ch, r8)) = make_uint4(ke[0], ke[1], ke[2], ke[3]);
-            }
+            const uint32_t off = sw128_off(r, cc);
+            *(uint4*)(opA + off) = pack8(km);
+            *(uint4*)(opA + sw128_off(64 + r, cc)) = pack8(qm);
+            if (!slow) *(uint4*)(opB1 + off) = pack8(kh);
+            *(uint4*)(ke + off) = pack8(kend);
         }
-        ((float*)(rec + TcRec::kGam))[ch] = exp2f(gC);
     }
     fence_proxy_async_smem();
     __syncthreads();
 
-    float* At = (float*)(sm + SmemA::kOpA);       // At[j][i] = A[i][j], fp32 [64][64] (after MMA-a)
-    float Y[kChunk];                              // row `tid` of [X; P X], X = (I + A)^-1
+    uint32_t mph = 0;                 // completed phases of bars[1]
+    bool abort = false;
     if (!slow) {
-        if (tid == 0 && !abort) {
-            // K^end^T image -> record (smem read by the copy engine, async)
-            bulk_s2g(rec + TcRec::kKE, sm + SmemA::kKE, 16384);
-            bulk_commit();
-            tc_fence_after_sync();
+        if (tid == 0) {
             const uint32_t id = idesc_bf16(128, 64);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -237,161 +366,145 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             mma_commit(&bars[1]);
         }
-        if (!abort && !mbar_wait(&bars[1], 0, kWaitNs)) { s_flag[1] = 1; }
+        if (!mbar_wait(&bars[1], mph & 1, kWaitNs)) s_flag[1] = 1;
+        ++mph;
         tc_fence_after_sync();
-        // D rows 0..63 (warps 0,1): Gram -> A^T; rows 64..127 (warps 2,3): P row in registers.
-        float d[kChunk];
-#pragma unroll
-        for (int c0 = 0; c0 < kChunk; c0 += 16) {
-            float f[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, c0), f);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) d[c0 + j] = f[j];
-        }
-        tc_fence_before_sync();
-        __syncthreads();                          // everyone done with MMA-a operands
-        if (warp < 2) {
-            const int i = tid;                    // token row of the Gram block
-            const float bi = s_beta[i];
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) At[j * kChunk + i] = (j < i) ? bi * d[j] : 0.f;
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) Y[j] = (j == i) ? 1.f : 0.f;
-        } else {
-            const int i = tid - 64;
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) Y[j] = (j <= i) ? d[j] : 0.f;
-        }
     } else {
-        // Slow path: g to shared memory (fp32 [64][128] over the LA/V tiles), then
-        // A and P on CUDA cores with exp(g_i - g_j) inside the sums.
-        float* gS = (float*)(sm + SmemA::kInLA);
+        // Rows of the Gram block (lane quarters 0,1) and of Q~ K^T (2,3) on CUDA
+        // cores with exp(g_i - g_j) <= 1 inside the sums, stored to TMEM.  The
+        // two warps of a lane quarter split the 64 columns.
+        const float* gS = (const float*)(sm + SmemA::kGS);
+        const int quarter = warp & 3, half = warp >> 2;
+        const int i = (quarter & 1) * 32 + lane;
+        const __nv_bfloat16* left = (quarter < 2 ? k : q) + ((size_t)(t0 + i) * H + h) * kTcD;
+#pragma unroll 1
+        for (int j0 = 32 * half; j0 < 32 * half + 32; j0 += 16) {
+            float f[16];
 #pragma unroll
-        for (int r = 0; r < kChunk; ++r) gS[r * kTcD + ch] = G[r];
-        if (tid == 0 && !abort) {
-            bulk_s2g(rec + TcRec::kKE, sm + SmemA::kKE, 16384);
-            bulk_commit();
-        }
-        __syncthreads();
-        float* Ps = (float*)(sm + SmemA::kOpA + 16384);   // P fp32 [64][64]
-        for (int e = tid; e < kChunk * kChunk; e += 128) {
-            const int i = e >> 6, j = e & 63;
-            float a = 0.f, p = 0.f;
-            if (j <= i && i < len) {
-                for (int cc = 0; cc < kTcD; ++cc) {
-                    const float ek = __bfloat162float(inK[j * kTcD + cc]) *
-                                     exp2f(gS[i * kTcD + cc] - gS[j * kTcD + cc]);
-                    a = fmaf(__bfloat162float(inK[i * kTcD + cc]), ek, a);
-                    p = fmaf(__bfloat162float(inQ[i * kTcD + cc]), ek, p);
+            for (int jj = 0; jj < 16; ++jj) {
+                const int j = j0 + jj;
+                float acc = 0.f;
+                if (j <= i && i < len) {
+                    const __nv_bfloat16* kj = k + ((size_t)(t0 + j) * H + h) * kTcD;
+#pragma unroll 1
+                    for (int c2 = 0; c2 < kTcD; ++c2)
+                        acc = fmaf(__bfloat162float(left[c2]) * __bfloat162float(kj[c2]),
+                                   exp2f(gS[i * kTcD + c2] - gS[j * kTcD + c2]), acc);
                 }
+                f[jj] = acc;
             }
-            At[j * kChunk + i] = (j < i) ? s_beta[i] * a : 0.f;
-            Ps[i * kChunk + j] = p;
+            tmem_st16(tmem_addr(tmem, 32 * quarter, j0), f);
         }
-        __syncthreads();
-        if (warp < 2) {
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) Y[j] = (j == tid) ? 1.f : 0.f;
-        } else {
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) Y[j] = Ps[(tid - 64) * kChunk + j];
-        }
+        tmem_wait_st();
     }
-    __syncthreads();                              // At complete
+    tc_fence_before_sync();
+    __syncthreads();                  // K^m (or g) no longer needed
+    tc_fence_after_sync();
+    abort = s_flag[1] != 0;
 
-    // ---- step 4: Y (I + A) = [I; P], columns from the right ----
+    // A^[i][j] = beta_j G[i][j] (j < i) row by row into the 16-column blocks
+    // (MN-major, rows m = i), and the diagonal blocks transposed into At32.
     {
-        const float4* At4 = (const float4*)At;
+        const int quarter = warp & 3, half = warp >> 2;
+        if (quarter < 2) {
+            const int i = quarter * 32 + lane, ii = i & 15;
+            float* at32 = (float*)(sm + SmemA::kAt32);
+#pragma unroll 1
+            for (int j0 = 32 * half; j0 < 32 * half + 32; j0 += 16) {
+                float f[16];
+                tmem_ld16(tmem_addr(tmem, 32 * quarter, j0), f);
+                tmem_wait_ld();
+                const bool diag = (j0 >> 4) == (i >> 4);
+                float a[16];
 #pragma unroll
-        for (int j = kChunk - 2; j >= 0; --j) {
-            float acc = Y[j];
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = j0 + jj;
+                    a[jj] = (j < i) ? s_beta[j] * f[jj] : 0.f;
+                    if (diag) at32[j * 16 + ii] = a[jj];
+                }
+                uint8_t* blk = sm + SmemA::kAt + (j0 >> 4) * 2048;
+                float lo[8], hi[8];
 #pragma unroll
-            for (int g4 = (j + 1) >> 2; g4 < kChunk / 4; ++g4) {
-                const float4 a = At4[j * (kChunk / 4) + g4];
-                if (4 * g4 + 0 > j) acc = fmaf(-Y[4 * g4 + 0], a.x, acc);
-                if (4 * g4 + 1 > j) acc = fmaf(-Y[4 * g4 + 1], a.y, acc);
-                if (4 * g4 + 2 > j) acc = fmaf(-Y[4 * g4 + 2], a.z, acc);
-                if (4 * g4 + 3 > j) acc = fmaf(-Y[4 * g4 + 3], a.w, acc);
+                for (int e = 0; e < 8; ++e) { lo[e] = a[e]; hi[e] = a[8 + e]; }
+                *(uint4*)(blk + sw32_off(i, 0)) = pack8(lo);
+                *(uint4*)(blk + sw32_off(i, 8)) = pack8(hi);
             }
-            Y[j] = acc;
-        }
-    }
-    // ---- step 5: row `tid` of [[T, 0], [P T, -I]] as the MMA-b A operand ----
-    {
-        uint8_t* opA2 = sm + SmemA::kInK;          // 2 K-blocks x [128 rows x 128 B] over the K/Q tiles
-        const int row = tid;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = c8 * 8 + 2 * e;
-                w4[e] = pack_bf16x2(Y[j] * s_beta[j], Y[j + 1] * s_beta[j + 1]);
-            }
-            *(uint4*)(opA2 + sw128_off(row, c8 * 8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            uint32_t z[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = c8 * 8 + 2 * e;
-                const float lo = (row >= 64 && row - 64 == j) ? -1.f : 0.f;
-                const float hi = (row >= 64 && row - 64 == j + 1) ? -1.f : 0.f;
-                z[e] = pack_bf16x2(lo, hi);
-            }
-            *(uint4*)(opA2 + 16384 + sw128_off(row, c8 * 8)) = make_uint4(z[0], z[1], z[2], z[3]);
         }
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    abort = abort || s_flag[1] != 0;
+
+    // ---- Y^ (I + A^) = [Diag(beta); P Diag(beta)], 16-column blocks from the right.
+    inv_block<3>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
+    inv_block<2>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
+    inv_block<1>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
+    inv_block<0>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
+
+    // ---- MMA-b: Y^ [K~m | V] -> [[W Em^-1, U0], [P T K~m, O0]].  Its issuing
+    // thread waits for the V tile first (the MMA reads it).
+    if (tid == 0 && !abort && !mbar_wait(&bars[0], 0, kWaitNs)) { s_flag[1] = 1; abort = true; }
     if (tid == 0 && !abort) {
-        const uint32_t id256 = idesc_bf16(128, 256), id128 = idesc_bf16(128, 128);
+        const uint32_t id = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kInK + ks * 32)),
-                        sdesc_k_sw128(smem_u32(sm + SmemA::kOpB2 + ks * 32)), id256, ks > 0);
+            mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
+                        sdesc(smem_u32(sm + SmemA::kOpA + ks * 2048), 16384, 1024, 2), id, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kInK + 16384 + ks * 32)),
-                        sdesc_k_sw128(smem_u32(sm + SmemA::kOpB2 + 32768 + ks * 32)), id128, 1);
+            mma_bf16_ss(tmem + 128, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
+                        sdesc(smem_u32(sm + SmemA::kV + ks * 2048), 8192, 1024, 2), id, ks > 0);
         mma_commit(&bars[1]);
     }
-    if (!abort && !mbar_wait(&bars[1], slow ? 0 : 1, kWaitNs)) s_flag[1] = 1;
+    __syncthreads();
+    abort = s_flag[1] != 0;
+    if (!abort && !mbar_wait(&bars[1], mph & 1, kWaitNs)) s_flag[1] = 1;
+    ++mph;
     tc_fence_after_sync();
+    __syncthreads();
+    abort = s_flag[1] != 0;
 
-    // ---- step 6: epilogue.  Warps 0,1: rows 0..63 = [W | U0]; warps 2,3: rows 64..127 = [-Q' | O0].
+    // ---- epilogue.  Lane quarters 0,1: rows 0..63 = [W | U0]; quarters 2,3:
+    // rows 64..127 = [P T K~ | O0].  The two warps of a quarter split columns.
     if (!abort) {
-        const int i = (warp & 1) * 32 + lane;      // token row within the chunk
-        const bool top = warp < 2;
+        const int quarter = warp & 3, half = warp >> 2;
+        const int i = (quarter & 1) * 32 + lane;      // token row within the chunk
+        const bool top = quarter < 2;
         uint8_t* a1 = rec + TcRec::kA1;
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 16) {
+        const uint8_t* qm = sm + SmemA::kOpA;
+#pragma unroll 1
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
             float f[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, c0), f);
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, c0), f);
             tmem_wait_ld();
-            const float sgn = top ? 1.f : -1.f;    // rows 64..127 hold -Q'
-            uint32_t p[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) p[e] = pack_bf16x2(sgn * f[2 * e], sgn * f[2 * e + 1]);
-            const int row = top ? i : 64 + i;
             const uint32_t kb = c0 >> 6, kin = c0 & 63;
-            *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin)) = make_uint4(p[0], p[1], p[2], p[3]);
-            *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = make_uint4(p[4], p[5], p[6], p[7]);
+            const int row = top ? i : 64 + i;
+            if (!top) {                                // Q' = (Q~m - P T K~m) Em
+                float q0[8], q1[8];
+                unpack8(*(const uint4*)(qm + kb * 16384 + sw128_off(row, kin)), q0);
+                unpack8(*(const uint4*)(qm + kb * 16384 + sw128_off(row, kin + 8)), q1);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { f[e] = q0[e] - f[e]; f[8 + e] = q1[e] - f[8 + e]; }
+            }
+            float lo[8], hi[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { lo[e] = f[e] * s_em[c0 + e]; hi[e] = f[8 + e] * s_em[c0 + 8 + e]; }
+            *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin)) = pack8(lo);
+            *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = pack8(hi);
         }
         uint8_t* uo = rec + (top ? TcRec::kU0 : TcRec::kO0);
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t) {
+#pragma unroll 1
+        for (int t = 4 * half; t < 4 * half + 4; ++t) {
             float f[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 128 + t * kTile), f);
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, 128 + t * kTile), f);
             tmem_wait_ld();
-            uint32_t p[8];
+            float lo[8], hi[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) p[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+            for (int e = 0; e < 8; ++e) { lo[e] = f[e]; hi[e] = f[8 + e]; }
             uint4* dst = (uint4*)(uo + t * TcRec::kTileBytes + i * (kTile * 2));
-            dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-            dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+            dst[0] = pack8(lo);
+            dst[1] = pack8(hi);
         }
     } else if (tid == 0) {
         record_status(hdr, KDA_ERR_TIMEOUT);
@@ -399,7 +512,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
-    if (tid == 0) bulk_wait_all();                // the K^end image store has read its smem
+    if (tid == 0) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
 }
 
 // ---------------------------------------------------------------------------
@@ -409,8 +522,8 @@ constexpr int kStages = 3;
 struct SmemB {
     static constexpr uint32_t kStageA1 = 0, kStageKE = 32768, kStageU0 = 49152, kStageO0 = 51200,
                               kStageGam = 53248, kStageBytes = 54272;       // 53 KB, 1024-aligned
-    static constexpr uint32_t kST = kStages * kStageBytes;                 // S^T operand, 2 x 2 KB
-    static constexpr uint32_t kUT = kST + 4096;                            // U^T operand, 2 KB
+    static constexpr uint32_t kST = kStages * kStageBytes;                 // S operand (MN-major), 4 KB
+    static constexpr uint32_t kUT = kST + 4096;                            // U operand (MN-major), 2 KB
     static constexpr uint32_t kMisc = kUT + 2048;                          // barriers etc.
     static constexpr uint32_t kBytes = kMisc + 256 + 1024;
     static constexpr uint32_t kTx = 32768 + 16384 + 2 * TcRec::kTileBytes + 512;
@@ -495,11 +608,12 @@ kda_tc_inter_chunk(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hd
         }
         uint8_t* ST = sm + SmemB::kST;
         uint8_t* UT = sm + SmemB::kUT;
-        auto write_ST = [&]() {
-            const uint32_t kb = (uint32_t)i >> 6, kin = (uint32_t)i & 63u;
+        auto write_ST = [&]() {       // S slice as an MN-major operand: row i, 16 contiguous columns
+            uint32_t p[8];
 #pragma unroll
-            for (int j = 0; j < kTile; ++j)
-                *(__nv_bfloat16*)(ST + kb * 2048 + sw128_off(j, kin)) = __float2bfloat16_rn(S[j]);
+            for (int e = 0; e < 8; ++e) p[e] = pack_bf16x2(S[2 * e], S[2 * e + 1]);
+            *(uint4*)(ST + mn16_off(i, 0)) = make_uint4(p[0], p[1], p[2], p[3]);
+            *(uint4*)(ST + mn16_off(i, 8)) = make_uint4(p[4], p[5], p[6], p[7]);
         };
         write_ST();
         fence_proxy_async_smem();
@@ -507,7 +621,8 @@ kda_tc_inter_chunk(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hd
         // Consumers meet only at barriers that AND a "still good" flag, so a
         // wait that timed out in any thread stops all of them together.
         bool ok = bar_and(128, true);
-        const uint32_t id = idesc_bf16(128, kTile);
+        const uint32_t id1 = idesc_bf16(128, kTile, 0, 1);    // [W; Q'] K-major, S MN-major
+        const uint32_t id3 = idesc_bf16(128, kTile, 1, 1);    // K^end MN-major, U MN-major
         for (int it = 0; it < nchunks; ++it) {
             const int s = it % kStages;
             uint8_t* st = sm + s * SmemB::kStageBytes;
@@ -518,7 +633,7 @@ kda_tc_inter_chunk(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hd
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t kb = ks >> 2, kin = ks & 3;
                     mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(st + SmemB::kStageA1 + kb * 16384 + kin * 32)),
-                                sdesc_k_sw128(smem_u32(ST + kb * 2048 + kin * 32)), id, ks > 0);
+                                sdesc(smem_u32(ST + ks * 512), 256, 128, 0), id1, ks > 0);
                 }
                 mma_commit(mbar1);
             }
@@ -529,22 +644,28 @@ kda_tc_inter_chunk(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hd
             tmem_wait_ld();
             const int tok = (warp & 1) * 32 + lane;
             if (warp < 2) {
-                // U = U0 - W S  -> U^T operand (row j, token tok)
-                const __nv_bfloat16* u0 = (const __nv_bfloat16*)(st + SmemB::kStageU0) + tok * kTile;
+                // U = U0 - W S  -> U operand (row tok, 16 contiguous columns)
+                const uint4* u0 = (const uint4*)(st + SmemB::kStageU0 + tok * (kTile * 2));
+                const uint4 a = u0[0], b = u0[1];
+                const uint32_t uu[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                uint32_t p[8];
 #pragma unroll
-                for (int j = 0; j < kTile; ++j)
-                    *(__nv_bfloat16*)(UT + sw128_off(j, tok)) = __float2bfloat16_rn(__bfloat162float(u0[j]) - d1[j]);
+                for (int e = 0; e < 8; ++e)
+                    p[e] = pack_bf16x2(bf_lo(uu[e]) - d1[2 * e], bf_hi(uu[e]) - d1[2 * e + 1]);
+                *(uint4*)(UT + mn16_off(tok, 0)) = make_uint4(p[0], p[1], p[2], p[3]);
+                *(uint4*)(UT + mn16_off(tok, 8)) = make_uint4(p[4], p[5], p[6], p[7]);
                 fence_proxy_async_smem();
             } else if (good) {
                 // O = O0 + Q' S  -> out
                 const int64_t t = seq0 + (int64_t)it * kChunk + tok;
                 if (t < seq1) {
-                    const __nv_bfloat16* o0 = (const __nv_bfloat16*)(st + SmemB::kStageO0) + tok * kTile;
+                    const uint4* o0 = (const uint4*)(st + SmemB::kStageO0 + tok * (kTile * 2));
+                    const uint4 a = o0[0], b = o0[1];
+                    const uint32_t oo[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                     uint32_t p[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        p[e] = pack_bf16x2(__bfloat162float(o0[2 * e]) + d1[2 * e],
-                                           __bfloat162float(o0[2 * e + 1]) + d1[2 * e + 1]);
+                        p[e] = pack_bf16x2(bf_lo(oo[e]) + d1[2 * e], bf_hi(oo[e]) + d1[2 * e + 1]);
                     uint4* dst = (uint4*)(out + ((size_t)t * H + h) * kTcD + col0);
                     dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
                     dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
@@ -556,8 +677,8 @@ kda_tc_inter_chunk(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hd
             if (tid == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ss(tmem + 16, sdesc_k_sw128(smem_u32(st + SmemB::kStageKE + ks * 32)),
-                                sdesc_k_sw128(smem_u32(UT + ks * 32)), id, ks > 0);
+                    mma_bf16_ss(tmem + 16, sdesc(smem_u32(st + SmemB::kStageKE + ks * 2048), 8192, 1024, 2),
+                                sdesc(smem_u32(UT + ks * 512), 256, 128, 0), id3, ks > 0);
                 mma_commit(mbar3);
             }
             good = mbar_wait(mbar3, it & 1, kWaitNs);
@@ -604,15 +725,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [T, H, 128] bf16 tensor, box = one (chunk, head) tile of 64 tokens x 128.
-static bool make_map(CUtensorMap* m, const void* base, int64_t T, int H) {
+// V [T, H, 128] bf16; box = 64 tokens x 64 channels of one head, 128-byte
+// swizzle (the MN-major operand layout of the second intra-chunk product).
+static bool make_v_map(CUtensorMap* m, const void* base, int64_t T, int H) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t gdim[3] = {(cuuint64_t)kTcD, (cuuint64_t)H, (cuuint64_t)T};
     cuuint64_t gstr[2] = {(cuuint64_t)kTcD * 2, (cuuint64_t)H * kTcD * 2};
-    cuuint32_t box[3] = {kTcD, 1, kChunk}, es[3] = {1, 1, 1};
+    cuuint32_t box[3] = {64, 1, kChunk}, es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstr, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -624,13 +746,11 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
                                   (int)SmemB::kBytes)) != cudaSuccess) return e;
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[0], stream)) != cudaSuccess) return e;
     if (a.chunks_ub > 0 && T > 0) {
-        CUtensorMap mq, mk, mv, ml;
-        if (!make_map(&mq, a.q, T, a.H) || !make_map(&mk, a.k, T, a.H) || !make_map(&mv, a.v, T, a.H) ||
-            !make_map(&ml, a.la, T, a.H))
-            return cudaErrorInvalidValue;
-        kda_tc_intra_chunk<<<dim3(a.chunks_ub, a.H), 128, SmemA::kBytes, stream>>>(
-            mq, mk, mv, ml, (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H,
-            (uint8_t*)a.recs);
+        CUtensorMap mv;
+        if (!make_v_map(&mv, a.v, T, a.H)) return cudaErrorInvalidValue;
+        kda_tc_intra_chunk<<<dim3(a.chunks_ub, a.H), kAThreads, SmemA::kBytes, stream>>>(
+            mv, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.la,
+            (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, (uint8_t*)a.recs);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[1], stream)) != cudaSuccess) return e;

@@ -158,6 +158,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&f)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Registers -> TMEM, same lane/column mapping as tmem_ld16.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&f)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(__float_as_uint(f[0])), "r"(__float_as_uint(f[1])), "r"(__float_as_uint(f[2])),
+                   "r"(__float_as_uint(f[3])), "r"(__float_as_uint(f[4])), "r"(__float_as_uint(f[5])),
+                   "r"(__float_as_uint(f[6])), "r"(__float_as_uint(f[7])), "r"(__float_as_uint(f[8])),
+                   "r"(__float_as_uint(f[9])), "r"(__float_as_uint(f[10])), "r"(__float_as_uint(f[11])),
+                   "r"(__float_as_uint(f[12])), "r"(__float_as_uint(f[13])), "r"(__float_as_uint(f[14])),
+                   "r"(__float_as_uint(f[15]))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // TMEM address of (lane, column) relative to an allocation base.
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
     return base + (lane << 16) + col;
@@ -177,19 +191,43 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
          | ((uint64_t)2 << 61);                     // 128-byte swizzle
 }
 
-// Instruction descriptor: kind::f16 with bf16 A/B, fp32 D, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+// General shared-memory matrix descriptor.  Swizzle codes: 0 none, 2 128-byte,
+// 4 64-byte, 6 32-byte.  For K-major operands with 128-byte swizzle the
+// leading offset is unused and the stride offset is the 8-row group pitch.  For
+// MN-major operands with swizzle the leading offset is the pitch between
+// swizzle atoms along M/N and the stride offset the pitch between 8-row K
+// groups; without swizzle the leading offset is the pitch between 8-row K
+// groups and the stride offset the pitch between 8-element M/N groups.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t swz) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | (swz << 61);
+}
+
+// Instruction descriptor: kind::f16 with bf16 A/B, fp32 D, M x N.  a_mn / b_mn
+// select an MN-major (1) instead of a K-major (0) operand.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn = 0, int b_mn = 0) {
     return (1u << 4)                     // D format: f32
          | (1u << 7)                     // A format: bf16
          | (1u << 10)                    // B format: bf16
+         | ((uint32_t)(a_mn & 1) << 15)  // A major-ness
+         | ((uint32_t)(b_mn & 1) << 16)  // B major-ness
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// Byte offset of element (row r, k) of a bf16 K-major tile with 128-byte rows
-// in the 128-byte-swizzle layout above (k < 64).
+// Byte offset of element (row r, column c < 64) of a bf16 tile with 128-byte
+// rows in the 128-byte-swizzle layout (the layout a TMA SWIZZLE_128B box of 64
+// bf16 columns produces).  As a K-major operand rows are M/N and columns K; as
+// an MN-major operand rows are K and columns M/N.
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t k) {
     return r * 128u + ((((k >> 3) ^ (r & 7u)) & 7u) << 4) + (k & 7u) * 2u;
+}
+
+// Byte offset of element (k, n < 16) of an N = 16 MN-major bf16 operand without
+// swizzle: 8-row K groups of two 8 x 16-byte core matrices (256 bytes per group).
+// Descriptor: leading offset 256, stride offset 128; +512 bytes per 16 K rows.
+__host__ __device__ __forceinline__ uint32_t mn16_off(uint32_t k, uint32_t n) {
+    return (k >> 3) * 256u + (n >> 3) * 128u + (k & 7u) * 16u + (n & 7u) * 2u;
 }
 
 }  // namespace sm100
