@@ -92,6 +92,7 @@ struct Layout {
     size_t table_off;      // int32 chunk_first[N+1]
     size_t rec_off;        // per-(chunk, head) records
     size_t rec_bytes;
+    size_t extra_off;      // path-specific scratch
     size_t total;
 };
 
@@ -102,7 +103,8 @@ static Layout layout_for(const kda_desc* d) {
     L.table_off = sizeof(DeviceHeader);
     L.rec_off = align_up(L.table_off + ((size_t)d->num_seqs + 1) * sizeof(int32_t), 1024);
     L.rec_bytes = prefill_record_bytes(L.path, d->d_k);
-    L.total = L.rec_off + (size_t)L.chunks_ub * d->num_heads * L.rec_bytes;
+    L.extra_off = align_up(L.rec_off + (size_t)L.chunks_ub * d->num_heads * L.rec_bytes, 1024);
+    L.total = L.extra_off + prefill_extra_bytes(L.path, d->num_seqs, d->num_heads, d->total_tokens);
     return L;
 }
 
@@ -199,7 +201,7 @@ int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
     a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.beta = beta;
     a.cu = cu_seqlens ? cu_seqlens : hdr->pad;
     a.s0 = initial_state; a.out = out; a.sf = final_state;
-    a.hdr = hdr; a.chunk_first = chunk_first; a.recs = ws + L.rec_off;
+    a.hdr = hdr; a.chunk_first = chunk_first; a.recs = ws + L.rec_off; a.extra = ws + L.extra_off;
     a.phase_events = (cudaEvent_t*)d->phase_events;
     e = prefill_launch(L.path, a, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -254,6 +256,10 @@ int choose_prefill_path(int dtype, int d, int flags) {
 
 size_t prefill_record_bytes(int path, int d) {
     return path == kPathTensorCore ? tc_record_bytes() : simt_record_bytes(d);
+}
+
+size_t prefill_extra_bytes(int path, int N, int H, int64_t T) {
+    return path == kPathTensorCore ? tc_extra_bytes(N, H, T) : 0;
 }
 
 cudaError_t prefill_launch(int path, const PrefillArgs& a, cudaStream_t stream) {

@@ -13,6 +13,8 @@ enum PrefillPath { kPathSimt = 0, kPathTensorCore = 1 };
 int choose_prefill_path(int dtype, int d, int flags);
 // Bytes of workspace per (chunk, head) record for a path.
 size_t prefill_record_bytes(int path, int d);
+// Bytes of path-specific scratch after the records.
+size_t prefill_extra_bytes(int path, int N, int H, int64_t T);
 
 // Launch arguments shared by the prefill paths.
 struct PrefillArgs {
@@ -26,6 +28,7 @@ struct PrefillArgs {
     void* hdr;                   // DeviceHeader in the workspace
     const int32_t* chunk_first;  // [N+1] chunk offsets in the workspace
     void* recs;                  // per-(chunk, head) records
+    void* extra;                 // path-specific scratch after the records
     cudaEvent_t* phase_events;   // optional timing events (3) or nullptr
 };
 
@@ -41,6 +44,7 @@ cudaError_t prefill_simt_launch(const PrefillArgs& a, cudaStream_t stream);
 
 // Tensor-core (tcgen05) prefill: bf16 inputs, head size 128.
 size_t tc_record_bytes();
+size_t tc_extra_bytes(int N, int H, int64_t T);
 cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stream);
 
 }  // namespace kda

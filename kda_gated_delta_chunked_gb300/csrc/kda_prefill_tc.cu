@@ -516,198 +516,325 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 }
 
 // ---------------------------------------------------------------------------
-// Kernel (b)
+// Kernel (b): the chain over chunks, one CTA per (sequence, head, segment)
 // ---------------------------------------------------------------------------
-constexpr int kStages = 3;
-struct SmemB {
-    static constexpr uint32_t kStageA1 = 0, kStageKE = 32768, kStageU0 = 49152, kStageO0 = 51200,
-                              kStageGam = 53248, kStageBytes = 54272;       // 53 KB, 1024-aligned
-    static constexpr uint32_t kST = kStages * kStageBytes;                 // S operand (MN-major), 4 KB
-    static constexpr uint32_t kUT = kST + 4096;                            // U operand (MN-major), 2 KB
-    static constexpr uint32_t kMisc = kUT + 2048;                          // barriers etc.
-    static constexpr uint32_t kBytes = kMisc + 256 + 1024;
-    static constexpr uint32_t kTx = 32768 + 16384 + 2 * TcRec::kTileBytes + 512;
+// Segments split one sequence's chunks so that long sequences occupy every SM:
+//   phase A (TRANS): each segment p but the last runs the chain from the
+//      augmented state X = [0 | I] (N = 256): it ends at [B_p | M_p], the
+//      affine map  S_end = M_p S_start + B_p  of the segment;
+//   phase B: S_start(p+1) = M_p S_start(p) + B_p, sequential over p, fp32;
+//   phase C (OUT): every segment from its true start state (N = 128), with the
+//      outputs; the last segment writes the final state.
+// A sequence that gets one segment is the plain chain (phase C only).
+// Planning uses a fixed SM count so that the workspace size depends on
+// (N, H, T) only.
+constexpr int kPlanSMs = 152;
+constexpr int kChainWarps = 16;                 // consumer warps (4 per TMEM lane quarter)
+constexpr int kChainThreads = 32 * kChainWarps + 32;
+
+struct ScanPlan {
+    int seg_chunks;   // chunks per segment
+    int segs_max;     // segments of the longest possible sequence
+};
+static ScanPlan scan_plan(int N, int H, int64_t T) {
+    ScanPlan p;
+    const int64_t chunks_max = (T + kChunk - 1) / kChunk;
+    int64_t target = (int64_t)N * H > 0 ? kPlanSMs / ((int64_t)N * H) : 1;
+    if (target < 1) target = 1;
+    int64_t seg = (chunks_max + target - 1) / target;
+    if (seg < 128) seg = 128;                      // short segments are not worth the extra passes
+    p.seg_chunks = (int)seg;
+    p.segs_max = (int)((chunks_max + seg - 1) / seg);
+    if (p.segs_max < 1) p.segs_max = 1;
+    return p;
+}
+// Segment scratch per (sequence, head, segment): [B_p | M_p] fp32 [128][256] and
+// S_start fp32 [128][128].
+constexpr size_t kSegMB = (size_t)kTcD * 256 * 4, kSegS = (size_t)kTcD * kTcD * 4, kSegBytes = kSegMB + kSegS;
+
+size_t tc_extra_bytes(int N, int H, int64_t T) {
+    const ScanPlan p = scan_plan(N, H, T);
+    return p.segs_max > 1 ? (size_t)N * H * p.segs_max * kSegBytes : 0;
+}
+
+template <int NX> struct SmemC {
+    static constexpr bool kOut = NX == 128;
+    static constexpr uint32_t kA1 = 0, kKE = 32768, kU0 = 49152, kO0 = 65536;
+    static constexpr uint32_t kGam = kOut ? 81920 : 65536;
+    static constexpr uint32_t kStageUsed = kGam + 512;
+    static constexpr uint32_t kStageBytes = (kStageUsed + 1023) / 1024 * 1024;
+    static constexpr uint32_t kX = 2 * kStageBytes;                 // X operand, MN-major, [128 x NX]
+    static constexpr uint32_t kU = kX + 128 * NX * 2;                // U operand, MN-major, [64 x NX]
+    static constexpr uint32_t kMisc = kOut ? kU + 64 * NX * 2 : kStageUsed;   // TRANS: slack of stage 0
+    static constexpr uint32_t kBytes = kU + 64 * NX * 2 + (kOut ? 256 : 0) + 1024;
+    static constexpr uint32_t kTx = kStageUsed;                      // bytes copied per stage
 };
 
-__global__ void __launch_bounds__(160, 1)
-kda_tc_inter_chunk(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr,
-                   const int32_t* __restrict__ chunk_first, int H, const uint8_t* __restrict__ recs,
-                   const float* __restrict__ initial_state, __nv_bfloat16* __restrict__ out,
-                   float* __restrict__ final_state) {
+// Byte offset of (row, col) in an MN-major 128-byte-swizzle operand whose
+// 64-column atoms hold `rows` rows each.
+__device__ __forceinline__ uint32_t mn_off(uint32_t row, uint32_t col, uint32_t rows) {
+    return (col >> 6) * rows * 128u + sw128_off(row, col & 63u);
+}
+
+template <int NX>
+__global__ void __launch_bounds__(kChainThreads, 1)
+kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, const int32_t* __restrict__ chunk_first,
+             int H, int seg_chunks, const uint8_t* __restrict__ recs, const float* __restrict__ initial_state,
+             __nv_bfloat16* __restrict__ out, float* __restrict__ final_state, uint8_t* __restrict__ segbuf,
+             int segs_max) {
+    using L = SmemC<NX>;
+    constexpr bool kOut = L::kOut;
+    constexpr int kCols = NX / 4;                      // columns per consumer warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t* full = (uint64_t*)(sm + SmemB::kMisc);            // [kStages]
-    uint64_t* empty = full + kStages;                           // [kStages]
-    uint64_t* mbar1 = empty + kStages;
-    uint64_t* mbar3 = mbar1 + 1;
-    uint32_t* s_tmem = (uint32_t*)(mbar3 + 1);
+    uint64_t* full = (uint64_t*)(sm + L::kMisc);     // [2]
+    uint64_t* empty = full + 2;                      // [2]
+    uint64_t* mbar = empty + 2;
+    uint32_t* s_tmem = (uint32_t*)(mbar + 1);
     int* s_abort = (int*)(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (hdr->status != KDA_OK) return;
-    const int nh = blockIdx.x, n = nh / H, h = nh % H;
-    const int col0 = blockIdx.y * kTile;
-    const int c_begin = chunk_first[n], nchunks = chunk_first[n + 1] - c_begin;
+    const int nh = blockIdx.x, n = nh / H, h = nh % H, p = blockIdx.y;
+    const int c_seq = chunk_first[n], nch = chunk_first[n + 1] - c_seq;
+    int segs = (nch + seg_chunks - 1) / seg_chunks;
+    if (segs < 1) segs = 1;
+    if (p >= segs || (!kOut && p >= segs - 1)) return;
+    const int cb = p * seg_chunks, ce = min(nch, cb + seg_chunks);    // chunk range within the sequence
+    const int nsteps = ce - cb;
     const int64_t seq0 = cu[n], seq1 = cu[n + 1];
+    uint8_t* seg = segbuf ? segbuf + ((size_t)nh * segs_max + p) * kSegBytes : nullptr;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        mbar_init(mbar1, 1);
-        mbar_init(mbar3, 1);
+        for (int s = 0; s < 2; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(mbar, 1);
         fence_mbar_init();
         *s_abort = 0;
     }
-    if (warp == 0) { tmem_alloc(s_tmem, 32); tmem_relinquish(); }
+    if (warp == 0) { tmem_alloc(s_tmem, 2 * NX); tmem_relinquish(); }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
 
-    if (warp == 4) {
+    if (warp == kChainWarps) {
         // ---------------- producer ----------------
         if (lane == 0) {
             int issued = 0;
-            for (int it = 0; it < nchunks; ++it) {
-                const int s = it % kStages;
-                if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, kWaitNs)) {
+            for (int it = 0; it < nsteps; ++it) {
+                const int s = it & 1;
+                if (it >= 2 && !mbar_wait(&empty[s], ((it >> 1) - 1) & 1, kWaitNs)) {
                     *(volatile int*)s_abort = 1;
                     break;
                 }
                 if (*(volatile int*)s_abort) break;
-                const uint8_t* rec = recs + ((size_t)(c_begin + it) * H + h) * TcRec::kBytes;
-                uint8_t* st = sm + s * SmemB::kStageBytes;
-                mbar_arrive_expect_tx(&full[s], SmemB::kTx);
-                bulk_g2s(st + SmemB::kStageA1, rec + TcRec::kA1, 32768, &full[s]);
-                bulk_g2s(st + SmemB::kStageKE, rec + TcRec::kKE, 16384, &full[s]);
-                bulk_g2s(st + SmemB::kStageU0, rec + TcRec::kU0 + blockIdx.y * TcRec::kTileBytes,
-                         TcRec::kTileBytes, &full[s]);
-                bulk_g2s(st + SmemB::kStageO0, rec + TcRec::kO0 + blockIdx.y * TcRec::kTileBytes,
-                         TcRec::kTileBytes, &full[s]);
-                bulk_g2s(st + SmemB::kStageGam, rec + TcRec::kGam, 512, &full[s]);
+                const uint8_t* rec = recs + ((size_t)(c_seq + cb + it) * H + h) * TcRec::kBytes;
+                uint8_t* st = sm + s * L::kStageBytes;
+                mbar_arrive_expect_tx(&full[s], L::kTx);
+                bulk_g2s(st + L::kA1, rec + TcRec::kA1, 32768, &full[s]);
+                bulk_g2s(st + L::kKE, rec + TcRec::kKE, 16384, &full[s]);
+                bulk_g2s(st + L::kU0, rec + TcRec::kU0, 16384, &full[s]);
+                if (kOut) bulk_g2s(st + L::kO0, rec + TcRec::kO0, 16384, &full[s]);
+                bulk_g2s(st + L::kGam, rec + TcRec::kGam, 512, &full[s]);
                 issued = it + 1;
             }
-            // Drain: every copy this warp issued has landed before the CTA may exit.
-            for (int it = issued - kStages < 0 ? 0 : issued - kStages; it < issued; ++it)
-                mbar_wait(&full[it % kStages], (it / kStages) & 1, kWaitNs);
+            for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
+                mbar_wait(&full[it & 1], (it >> 1) & 1, kWaitNs);
         }
     } else {
-        // ---------------- consumers: thread i = key channel i ----------------
-        const int i = tid;
-        const size_t sbase = (size_t)nh * kTcD * kTcD + (size_t)i * kTcD + col0;
-        float S[kTile];
-        if (initial_state) {
-            const float4* p = (const float4*)(initial_state + sbase);
+        // ---------------- consumers: rows 32q..32q+31, columns [col0, col0 + kCols) ----------------
+        const int q = warp & 3, g = warp >> 2;
+        const int i = 32 * q + lane;                 // key channel (row of S / X)
+        const int tok = (q & 1) * 32 + lane;          // token row of the U / O halves
+        const int col0 = g * kCols;
+        float X[kCols];
+        if (kOut) {
+            const float* src = (p == 0) ? initial_state + ((size_t)nh * kTcD + i) * kTcD
+                                        : (const float*)(seg + kSegMB) + (size_t)i * kTcD;
+            if (p == 0 && !initial_state) {
 #pragma unroll
-            for (int q4 = 0; q4 < kTile / 4; ++q4) {
-                const float4 v = p[q4];
-                S[4 * q4] = v.x; S[4 * q4 + 1] = v.y; S[4 * q4 + 2] = v.z; S[4 * q4 + 3] = v.w;
+                for (int j = 0; j < kCols; ++j) X[j] = 0.f;
+            } else {
+#pragma unroll
+                for (int j = 0; j < kCols; j += 4) {
+                    const float4 v = *(const float4*)(src + col0 + j);
+                    X[j] = v.x; X[j + 1] = v.y; X[j + 2] = v.z; X[j + 3] = v.w;
+                }
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < kTile; ++j) S[j] = 0.f;
+            for (int j = 0; j < kCols; ++j) X[j] = (col0 + j == kTcD + i) ? 1.f : 0.f;   // [0 | I]
         }
-        uint8_t* ST = sm + SmemB::kST;
-        uint8_t* UT = sm + SmemB::kUT;
-        auto write_ST = [&]() {       // S slice as an MN-major operand: row i, 16 contiguous columns
-            uint32_t p[8];
+        uint8_t* XO = sm + L::kX;
+        uint8_t* UO = sm + L::kU;
+        auto write_X = [&](float gam) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) p[e] = pack_bf16x2(S[2 * e], S[2 * e + 1]);
-            *(uint4*)(ST + mn16_off(i, 0)) = make_uint4(p[0], p[1], p[2], p[3]);
-            *(uint4*)(ST + mn16_off(i, 8)) = make_uint4(p[4], p[5], p[6], p[7]);
+            for (int j = 0; j < kCols; j += 8) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = gam * X[j + e];
+                *(uint4*)(XO + mn_off(i, col0 + j, 128)) = pack8(v);
+            }
         };
-        write_ST();
+        const uint32_t id1 = idesc_bf16(128, NX, 0, 1);     // [W; Q'] K-major, X MN-major
+        const uint32_t id3 = idesc_bf16(128, NX, 1, 1);     // K^end MN-major, U MN-major
+        uint32_t ph = 0;
+        write_X(1.f);
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        // Consumers meet only at barriers that AND a "still good" flag, so a
-        // wait that timed out in any thread stops all of them together.
-        bool ok = bar_and(128, true);
-        const uint32_t id1 = idesc_bf16(128, kTile, 0, 1);    // [W; Q'] K-major, S MN-major
-        const uint32_t id3 = idesc_bf16(128, kTile, 1, 1);    // K^end MN-major, U MN-major
-        for (int it = 0; it < nchunks; ++it) {
-            const int s = it % kStages;
-            uint8_t* st = sm + s * SmemB::kStageBytes;
-            bool good = mbar_wait(&full[s], (it / kStages) & 1, kWaitNs);
+        bool ok = bar_and(32 * kChainWarps, true);
+        for (int it = 0; it < nsteps && ok; ++it) {
+            const int s = it & 1;
+            const uint8_t* st = sm + s * L::kStageBytes;
+            bool good = mbar_wait(&full[s], (it >> 1) & 1, kWaitNs);
             tc_fence_after_sync();
             if (tid == 0 && good) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t kb = ks >> 2, kin = ks & 3;
-                    mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(st + SmemB::kStageA1 + kb * 16384 + kin * 32)),
-                                sdesc(smem_u32(ST + ks * 512), 256, 128, 0), id1, ks > 0);
+                    mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(st + L::kA1 + kb * 16384 + kin * 32)),
+                                sdesc(smem_u32(XO + ks * 2048), 16384, 1024, 2), id1, ks > 0);
                 }
-                mma_commit(mbar1);
+                mma_commit(mbar);
             }
-            good = good && mbar_wait(mbar1, it & 1, kWaitNs);
+            good = good && mbar_wait(mbar, ph & 1, kWaitNs);
+            ++ph;
             tc_fence_after_sync();
-            float d1[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 0), d1);
-            tmem_wait_ld();
-            const int tok = (warp & 1) * 32 + lane;
-            if (warp < 2) {
-                // U = U0 - W S  -> U operand (row tok, 16 contiguous columns)
-                const uint4* u0 = (const uint4*)(st + SmemB::kStageU0 + tok * (kTile * 2));
-                const uint4 a = u0[0], b = u0[1];
-                const uint32_t uu[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                uint32_t p[8];
+            if (q < 2) {
+                // U = U0 - W X  (the M columns have no U0 term)
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    p[e] = pack_bf16x2(bf_lo(uu[e]) - d1[2 * e], bf_hi(uu[e]) - d1[2 * e + 1]);
-                *(uint4*)(UT + mn16_off(tok, 0)) = make_uint4(p[0], p[1], p[2], p[3]);
-                *(uint4*)(UT + mn16_off(tok, 8)) = make_uint4(p[4], p[5], p[6], p[7]);
+                for (int j = 0; j < kCols; j += 16) {
+                    float d[16];
+                    tmem_ld16(tmem_addr(tmem, 32 * q, col0 + j), d);
+                    tmem_wait_ld();
+                    const int c = col0 + j;
+                    float lo[8], hi[8];
+                    if (c < kTcD) {
+                        const uint8_t* u0 = st + L::kU0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2);
+                        float a[8], b[8];
+                        unpack8(*(const uint4*)u0, a);
+                        unpack8(*(const uint4*)(u0 + 16), b);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) { lo[e] = a[e] - d[e]; hi[e] = b[e] - d[8 + e]; }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) { lo[e] = -d[e]; hi[e] = -d[8 + e]; }
+                    }
+                    *(uint4*)(UO + mn_off(tok, c, 64)) = pack8(lo);
+                    *(uint4*)(UO + mn_off(tok, c + 8, 64)) = pack8(hi);
+                }
                 fence_proxy_async_smem();
-            } else if (good) {
-                // O = O0 + Q' S  -> out
-                const int64_t t = seq0 + (int64_t)it * kChunk + tok;
-                if (t < seq1) {
-                    const uint4* o0 = (const uint4*)(st + SmemB::kStageO0 + tok * (kTile * 2));
-                    const uint4 a = o0[0], b = o0[1];
-                    const uint32_t oo[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                    uint32_t p[8];
+            } else if (kOut) {
+                // O = O0 + Q' S -> out.  The TMEM loads are warp-collective: every
+                // lane takes part, only the stores of real tokens are predicated.
+                const int64_t t = seq0 + (int64_t)(cb + it) * kChunk + tok;
+                const bool store = good && t < seq1;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        p[e] = pack_bf16x2(bf_lo(oo[e]) + d1[2 * e], bf_hi(oo[e]) + d1[2 * e + 1]);
-                    uint4* dst = (uint4*)(out + ((size_t)t * H + h) * kTcD + col0);
-                    dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                    dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                for (int j = 0; j < kCols; j += 16) {
+                    float d[16];
+                    tmem_ld16(tmem_addr(tmem, 32 * q, col0 + j), d);
+                    tmem_wait_ld();
+                    const int c = col0 + j;
+                    const uint8_t* o0 = st + L::kO0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2);
+                    float a[8], b[8];
+                    unpack8(*(const uint4*)o0, a);
+                    unpack8(*(const uint4*)(o0 + 16), b);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { a[e] += d[e]; b[e] += d[8 + e]; }
+                    if (store) {
+                        uint4* dst = (uint4*)(out + ((size_t)t * H + h) * kTcD + c);
+                        dst[0] = pack8(a);
+                        dst[1] = pack8(b);
+                    }
                 }
             }
             tc_fence_before_sync();
-            if (!bar_and(128, good)) { ok = false; break; }
+            if (!bar_and(32 * kChainWarps, good)) { ok = false; break; }
             tc_fence_after_sync();
             if (tid == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ss(tmem + 16, sdesc(smem_u32(st + SmemB::kStageKE + ks * 2048), 8192, 1024, 2),
-                                sdesc(smem_u32(UT + ks * 512), 256, 128, 0), id3, ks > 0);
-                mma_commit(mbar3);
+                    mma_bf16_ss(tmem + NX, sdesc(smem_u32(st + L::kKE + ks * 2048), 8192, 1024, 2),
+                                sdesc(smem_u32(UO + ks * 2048), 8192, 1024, 2), id3, ks > 0);
+                mma_commit(mbar);
             }
-            good = mbar_wait(mbar3, it & 1, kWaitNs);
+            good = mbar_wait(mbar, ph & 1, kWaitNs);
+            ++ph;
             tc_fence_after_sync();
-            float d3[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 16), d3);
-            tmem_wait_ld();
-            const float gam = ((const float*)(st + SmemB::kStageGam))[i];
+            const float gam = ((const float*)(st + L::kGam))[i];
 #pragma unroll
-            for (int j = 0; j < kTile; ++j) S[j] = fmaf(gam, S[j], d3[j]);
-            write_ST();
+            for (int j = 0; j < kCols; j += 16) {
+                float d[16];
+                tmem_ld16(tmem_addr(tmem, 32 * q, NX + col0 + j), d);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) X[j + e] = fmaf(gam, X[j + e], d[e]);
+            }
+            write_X(1.f);
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            if (!bar_and(128, good)) { ok = false; break; }
-            if (tid == 0) mbar_arrive(&empty[s]);
+            ok = bar_and(32 * kChainWarps, good);
+            if (ok && tid == 0) mbar_arrive(&empty[s]);
         }
         if (!ok) {
             *(volatile int*)s_abort = 1;
             if (tid == 0) record_status(hdr, KDA_ERR_TIMEOUT);
-        } else if (final_state) {
-            float4* p = (float4*)(final_state + sbase);
+        } else if (kOut) {
+            if (p == segs - 1 && final_state) {
+                float* dst = final_state + ((size_t)nh * kTcD + i) * kTcD + col0;
 #pragma unroll
-            for (int q4 = 0; q4 < kTile / 4; ++q4)
-                p[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+                for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
+            }
+        } else {
+            float* dst = (float*)seg + (size_t)i * 256 + col0;
+#pragma unroll
+            for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
         }
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 32);
+    if (warp == 0) tmem_dealloc(tmem, 2 * NX);
+}
+
+// Phase B: S_start(p+1) = M_p S_start(p) + B_p for one (sequence, head) and a
+// 16-column block of the state (columns of S are independent), fp32.
+__global__ void __launch_bounds__(256)
+kda_tc_scan_states(const int32_t* __restrict__ chunk_first, DeviceHeader* __restrict__ hdr, int H, int seg_chunks,
+                   const float* __restrict__ initial_state, uint8_t* __restrict__ segbuf, int segs_max) {
+    if (hdr->status != KDA_OK) return;
+    const int nh = blockIdx.x, n = nh / H, cblk = blockIdx.y * 16;
+    const int nch = chunk_first[n + 1] - chunk_first[n];
+    const int segs = (nch + seg_chunks - 1) / seg_chunks;
+    if (segs < 2) return;
+    __shared__ float S[kTcD][16];
+    const int tid = threadIdx.x, row = tid >> 1, half = (tid & 1) * 8;
+    for (int e = tid; e < kTcD * 16; e += 256) {
+        const int r = e >> 4, cc = e & 15;
+        S[r][cc] = initial_state ? initial_state[((size_t)nh * kTcD + r) * kTcD + cblk + cc] : 0.f;
+    }
+    __syncthreads();
+    for (int p = 0; p + 1 < segs; ++p) {
+        const float* MB = (const float*)(segbuf + ((size_t)nh * segs_max + p) * kSegBytes);
+        const float* Mrow = MB + (size_t)row * 256 + kTcD;       // M_p row `row`
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = MB[(size_t)row * 256 + cblk + half + e];   // B_p
+        for (int kk = 0; kk < kTcD; kk += 4) {
+            const float4 m = *(const float4*)(Mrow + kk);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] += m.x * S[kk][half + e] + m.y * S[kk + 1][half + e] + m.z * S[kk + 2][half + e] +
+                          m.w * S[kk + 3][half + e];
+        }
+        __syncthreads();
+        float* Snext = (float*)(segbuf + ((size_t)nh * segs_max + p + 1) * kSegBytes + kSegMB);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            S[row][half + e] = acc[e];
+            Snext[(size_t)row * kTcD + cblk + half + e] = acc[e];
+        }
+        __syncthreads();
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -742,8 +869,10 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(kda_tc_intra_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)SmemA::kBytes)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(kda_tc_inter_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)SmemB::kBytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kda_tc_chain<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)SmemC<128>::kBytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kda_tc_chain<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)SmemC<256>::kBytes)) != cudaSuccess) return e;
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[0], stream)) != cudaSuccess) return e;
     if (a.chunks_ub > 0 && T > 0) {
         CUtensorMap mv;
@@ -754,8 +883,21 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[1], stream)) != cudaSuccess) return e;
-    kda_tc_inter_chunk<<<dim3((unsigned)a.N * a.H, kTiles), 160, SmemB::kBytes, stream>>>(
-        a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.H, (const uint8_t*)a.recs, a.s0, (__nv_bfloat16*)a.out, a.sf);
+    const ScanPlan plan = scan_plan(a.N, a.H, T);
+    uint8_t* segbuf = plan.segs_max > 1 ? (uint8_t*)a.extra : nullptr;
+    const dim3 grid((unsigned)a.N * a.H, plan.segs_max);
+    if (segbuf) {
+        kda_tc_chain<256><<<grid, kChainThreads, SmemC<256>::kBytes, stream>>>(
+            a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.H, plan.seg_chunks, (const uint8_t*)a.recs, a.s0,
+            (__nv_bfloat16*)a.out, a.sf, segbuf, plan.segs_max);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        kda_tc_scan_states<<<dim3((unsigned)a.N * a.H, kTcD / 16), 256, 0, stream>>>(
+            a.chunk_first, (DeviceHeader*)a.hdr, a.H, plan.seg_chunks, a.s0, segbuf, plan.segs_max);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    kda_tc_chain<128><<<grid, kChainThreads, SmemC<128>::kBytes, stream>>>(
+        a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.H, plan.seg_chunks, (const uint8_t*)a.recs, a.s0,
+        (__nv_bfloat16*)a.out, a.sf, segbuf, plan.segs_max);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[2], stream)) != cudaSuccess) return e;
     return cudaSuccess;

@@ -206,3 +206,23 @@ def test_tensor_core_path_matches_cuda_core_path(kda):
     assert rel_l2(host(s_tc), host(s_cc)) < 1e-2
     ro, rs = run_oracle(d)
     assert_parity("cuda-core path", host(o_cc), ro, host(s_cc), rs, "bf16")
+
+
+def test_segment_scan_single_long_sequence(kda):
+    """A sequence long enough to be split into segments (three segments of 128
+    chunks here): the per-segment transitions, their sequential combination and
+    the rerun from each segment's start state must reproduce the recurrence."""
+    w = custom(17, [24576], 2, 128, "bf16", la_lo=0.0001, la_hi=0.05)
+    d = prefill_inputs(w)
+    out, sf, _, _ = run_gpu(kda, d)
+    ro, rs = run_oracle(d)
+    assert_parity("segment scan", host(out), ro, host(sf), rs, "bf16")
+
+
+def test_segment_scan_mixed_lengths(kda):
+    """One sequence split into segments next to short ones that are not."""
+    w = custom(18, [20000, 300, 0, 64], 2, 128, "bf16", la_lo=0.0001, la_hi=0.02)
+    d = prefill_inputs(w)
+    out, sf, _, _ = run_gpu(kda, d)
+    ro, rs = run_oracle(d)
+    assert_parity("segment scan, mixed", host(out), ro, host(sf), rs, "bf16")
