@@ -487,9 +487,14 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 #pragma unroll
                 for (int e = 0; e < 8; ++e) { f[e] = q0[e] - f[e]; f[8 + e] = q1[e] - f[8 + e]; }
             }
-            float lo[8], hi[8];
+            float lo[8], hi[8], em[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) { lo[e] = f[e] * s_em[c0 + e]; hi[e] = f[8 + e] * s_em[c0 + 8 + e]; }
+            for (int e4 = 0; e4 < 4; ++e4) {
+                const float4 m = ((const float4*)(s_em + c0))[e4];
+                em[4 * e4] = m.x; em[4 * e4 + 1] = m.y; em[4 * e4 + 2] = m.z; em[4 * e4 + 3] = m.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { lo[e] = f[e] * em[e]; hi[e] = f[8 + e] * em[8 + e]; }
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin)) = pack8(lo);
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = pack8(hi);
         }
@@ -567,7 +572,9 @@ template <int NX> struct SmemC {
     static constexpr uint32_t kU = kX + 128 * NX * 2;                // U operand, MN-major, [64 x NX]
     static constexpr uint32_t kMisc = kOut ? kU + 64 * NX * 2 : kStageUsed;   // TRANS: slack of stage 0
     static constexpr uint32_t kBytes = kU + 64 * NX * 2 + (kOut ? 256 : 0) + 1024;
-    static constexpr uint32_t kTx = kStageUsed;                      // bytes copied per stage
+    static constexpr uint32_t kTx = kOut ? kStageUsed : kStageUsed - 16384;   // bytes copied per stage
+    // (the transition copies only the W half of [W; Q']; rows 64..127 of its MMA
+    //  accumulator then hold garbage and are never read)
 };
 
 // Byte offset of (row, col) in an MN-major 128-byte-swizzle operand whose
@@ -631,7 +638,12 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
                 const uint8_t* rec = recs + ((size_t)(c_seq + cb + it) * H + h) * TcRec::kBytes;
                 uint8_t* st = sm + s * L::kStageBytes;
                 mbar_arrive_expect_tx(&full[s], L::kTx);
-                bulk_g2s(st + L::kA1, rec + TcRec::kA1, 32768, &full[s]);
+                if (kOut) {
+                    bulk_g2s(st + L::kA1, rec + TcRec::kA1, 32768, &full[s]);
+                } else {   // the transition needs W only: rows 0..63 of both K-blocks
+                    bulk_g2s(st + L::kA1, rec + TcRec::kA1, 8192, &full[s]);
+                    bulk_g2s(st + L::kA1 + 16384, rec + TcRec::kA1 + 16384, 8192, &full[s]);
+                }
                 bulk_g2s(st + L::kKE, rec + TcRec::kKE, 16384, &full[s]);
                 bulk_g2s(st + L::kU0, rec + TcRec::kU0, 16384, &full[s]);
                 if (kOut) bulk_g2s(st + L::kO0, rec + TcRec::kO0, 16384, &full[s]);
