@@ -355,10 +355,18 @@ def bench_decode(kda, args, dev, stream, peaks, peak_src):
 
 
 def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
-    """Same metric through the public C ABI with pinned HOST buffers: every step
-    copies its inputs host->device, runs prefill + the decode hand-off, and
-    reads the outputs and final state back device->host."""
+    """Same metric through the public C ABI with pinned HOST buffers.  Every
+    step copies all inputs host->device, runs the prefill plus the decode
+    hand-off, and reads the outputs and final state back device->host.  The
+    sequence is processed in `pieces` consecutive calls, each continuing from
+    the previous call's final state in place (the state hand-off the API
+    exposes), so that the copies of one piece overlap the compute of the next
+    on separate streams."""
     T, H, D = w.total_tokens, w.num_heads, w.d_k
+    pieces = max(1, args.e2e_pieces)
+    while T % (pieces * 64):
+        pieces -= 1
+    tp = T // pieces
     hx = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in NAMES}
     for n in NAMES:
         hx[n].copy_(x[n])
@@ -368,28 +376,53 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
     hsf = torch.empty((1, H, D, D), dtype=torch.float32).pin_memory()
     hho = torch.empty((1, H, D), dtype=w.torch_dtype).pin_memory()
     dx = {n: torch.empty_like(x[n]) for n in NAMES}
-    ds0 = torch.empty_like(s0)
+    dst = torch.empty_like(s0)
     dout = torch.empty((T, H, D), dtype=w.torch_dtype, device=dev)
-    dsf = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
     dho = torch.empty((1, H, D), dtype=w.torch_dtype, device=dev)
+    pdesc = kda.make_desc(1, H, D, D, tp, w.torch_dtype)
+    pws = torch.empty(kda.kda_prefill_workspace_bytes(pdesc), dtype=torch.uint8, device=dev)
+    pdesc = kda.make_desc(1, H, D, D, tp, w.torch_dtype, pws)
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     h2d = sum(hx[n].numel() * hx[n].element_size() for n in NAMES) + hs0.numel() * 4
     d2h = hout.numel() * hout.element_size() + hsf.numel() * 4 + hho.numel() * hho.element_size()
-    desc.phase_events = None
 
     def step():
-        for n in NAMES:
-            dx[n].copy_(hx[n], non_blocking=True)
-        ds0.copy_(hs0, non_blocking=True)
-        rc = kda.kda_prefill(desc, dx["q"], dx["k"], dx["v"], dx["log_alpha"], dx["beta"], None, ds0, dout,
-                             dsf, stream)
-        if rc:
-            raise kda.KdaError("kda_prefill", rc)
-        rc = kda.kda_decode_step(ddesc, *(hand[n] for n in NAMES), dsf, dho, stream)
+        h2d_s.wait_stream(stream)          # the previous step no longer reads the device inputs
+        with torch.cuda.stream(h2d_s):
+            dst.copy_(hs0, non_blocking=True)
+        ev_in, ev_out = [], []
+        for k in range(pieces):
+            a, b = k * tp, (k + 1) * tp
+            with torch.cuda.stream(h2d_s):
+                for n in NAMES:
+                    dx[n][a:b].copy_(hx[n][a:b], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(h2d_s)
+                ev_in.append(e)
+        for k in range(pieces):
+            a, b = k * tp, (k + 1) * tp
+            stream.wait_event(ev_in[k])
+            rc = kda.kda_prefill(pdesc, dx["q"][a:b], dx["k"][a:b], dx["v"][a:b], dx["log_alpha"][a:b],
+                                 dx["beta"][a:b], None, dst, dout[a:b], dst, stream)
+            if rc:
+                raise kda.KdaError("kda_prefill", rc)
+            e = torch.cuda.Event()
+            e.record(stream)
+            ev_out.append(e)
+        rc = kda.kda_decode_step(ddesc, *(hand[n] for n in NAMES), dst, dho, stream)
         if rc:
             raise kda.KdaError("kda_decode_step", rc)
-        hout.copy_(dout, non_blocking=True)
-        hsf.copy_(dsf, non_blocking=True)
-        hho.copy_(dho, non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(stream)
+        with torch.cuda.stream(d2h_s):
+            for k in range(pieces):
+                a, b = k * tp, (k + 1) * tp
+                d2h_s.wait_event(ev_out[k])
+                hout[a:b].copy_(dout[a:b], non_blocking=True)
+            d2h_s.wait_event(done)
+            hsf.copy_(dst, non_blocking=True)
+            hho.copy_(dho, non_blocking=True)
+        stream.wait_stream(d2h_s)
 
     step()
     torch.cuda.synchronize()
@@ -406,7 +439,9 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
     ms = t0.elapsed_time(t1) / steps
     return {"value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall * 1e3, 3),
-            "steps": steps, "host_buffers": "pinned"}
+            "steps": steps, "host_buffers": "pinned",
+            "pieces": pieces, "schedule": "H2D, prefill continuation and D2H of consecutive pieces overlap "
+                                          "on three streams"}
 
 
 def cpu_baseline(w, seconds):
@@ -484,6 +519,7 @@ def main():
     ap.add_argument("--workload", type=int, default=4)
     ap.add_argument("--decode-reps", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-pieces", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=2048)
     ap.add_argument("--no-decode", action="store_true")
