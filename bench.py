@@ -18,6 +18,7 @@ max-over-ranks of the elapsed time bracket the timed region.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -178,6 +179,28 @@ def prefill_units(C=64, d=128, esz=2):
     return intra_flops, chain_flops, in_bytes, out_bytes
 
 
+def bench_workload(args):
+    """The prefill workload of the step; ``--tokens T`` keeps its distributions
+    and heads but makes it one sequence of T tokens (a smaller profiling case)."""
+    w = workload(args.workload)
+    if args.tokens:
+        w = dataclasses.replace(w, seqlens=[int(args.tokens)], name=f"{w.name}@T{int(args.tokens)}")
+    return w
+
+
+def prefill_launches(N, H, T, C=64, plan_sms=152, min_seg=128):
+    """Kernels one bf16 d=128 prefill launches: the sequence table, the
+    intra-chunk kernel, then either the inter-chunk pass alone or, when a
+    sequence is long enough to be cut into segments (one per SM share, at
+    least 128 chunks each), the transition pass, the state scan and the output
+    pass."""
+    chunks = -(-T // C)
+    target = max(1, plan_sms // max(1, N * H))
+    seg = max(min_seg, -(-chunks // target))
+    segs = max(1, -(-chunks // seg))
+    return 2 + (3 if segs > 1 else 1)
+
+
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
@@ -188,7 +211,7 @@ def run_ours(args, dist: Dist):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     peaks, peak_src = load_peaks()
-    w = workload(args.workload)
+    w = bench_workload(args)
     T, H, D = w.total_tokens, w.num_heads, w.d_k
 
     files = kda.prefill_kernel_files(w.dtype, D)
@@ -293,7 +316,7 @@ def run_ours(args, dist: Dist):
         "roofline": roofline,
         "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items() if kk != "files"}
                     for k, v in kinfo.items()},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (prefill_launches(1, H, T) + 1) * args.steps,
         "clocks": clocks,
     }
 
@@ -479,7 +502,7 @@ def cpu_baseline(w, seconds):
 # ----------------------------------------------------------------------------
 def run_reference(args):
     import oracle
-    w = workload(args.workload)
+    w = bench_workload(args)
     n_tok = args.ref_tokens
     chunks = [prefill_inputs(w, t_range=(i * n_tok, (i + 1) * n_tok)) for i in range(2)]
     s0 = chunks[0]["initial_state"]
@@ -517,6 +540,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="one sequence of this many tokens with the workload's distributions (profiling case)")
     ap.add_argument("--decode-reps", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-pieces", type=int, default=8)

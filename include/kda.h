@@ -24,6 +24,7 @@
  *  - Layouts: q, k, log_alpha [T_tot, H, d_k]; v, out [T_tot, H, d_v];
  *    beta [T_tot, H]; cu_seqlens int32 [N+1]; states fp32 [N, H, d_k, d_v]
  *    (d_v contiguous).  The decode step uses the same layouts with T_tot = N.
+ *    With KDA_FLAG_SCALAR_GATE, log_alpha is [T_tot, H] instead.
  *  - dtype (KDA_F32 or KDA_BF16) applies to q, k, v, log_alpha, beta and out;
  *    states are always fp32; all accumulation is fp32.
  *  - alpha = exp(log_alpha) is formed inside the kernels; beta is taken as
@@ -77,7 +78,15 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 enum {
     /* Run the prefill on CUDA cores in fp32 even where the tensor-core path
        applies (bf16, head size 128).  Slower; meant for cross-checking. */
-    KDA_FLAG_CUDA_CORE_PREFILL = 1
+    KDA_FLAG_CUDA_CORE_PREFILL = 1,
+    /* Scalar gate: log_alpha holds ONE value per (token, head) -- layout
+       [T_tot, H] for the prefill, [N, H] for the decode step, aligned to its
+       element size like beta -- and every key channel of the head decays by
+       that same alpha.  This is the Gated DeltaNet gate that KDA refines into
+       a per-channel one (deep dive, section 03: Gated DeltaNet multiplies a
+       head's state by a scalar alpha, KDA by Diag(alpha)); the result equals
+       the per-channel operator with log_alpha broadcast over d_k. */
+    KDA_FLAG_SCALAR_GATE = 2
 };
 
 /* Problem description.  Not retained by the library after a call returns. */
@@ -88,7 +97,7 @@ typedef struct kda_desc {
     int32_t d_v;            /* value head size: must equal d_k */
     int64_t total_tokens;   /* T_tot = cu_seqlens[N] (decode: must equal N) */
     int32_t dtype;          /* kda_dtype of q, k, v, log_alpha, beta, out */
-    int32_t flags;          /* 0 or KDA_FLAG_CUDA_CORE_PREFILL */
+    int32_t flags;          /* OR of KDA_FLAG_* bits (0: tensor cores where they apply, per-channel gate) */
     void *workspace;        /* device scratch owned by the caller (prefill only), 256-byte aligned */
     size_t workspace_bytes; /* its size in bytes */
     void **phase_events;    /* optional timing hook (NULL: none): kda_prefill records
@@ -112,6 +121,7 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_desc *desc);
  * parallel KDA"; variable-length batching per the FlashKDA update there).
  *
  *   q, k, log_alpha  [T_tot, H, d_k]   inputs, dtype `desc->dtype`
+ *                    (log_alpha [T_tot, H] with KDA_FLAG_SCALAR_GATE)
  *   v                [T_tot, H, d_v]
  *   beta             [T_tot, H]
  *   cu_seqlens       int32 [N+1], device; sequence n is packed tokens
@@ -190,6 +200,16 @@ KDA_API int kda_prefill_noalloc(const kda_desc *desc,
                                 const void *log_alpha, const void *beta,
                                 const int32_t *cu_seqlens, const float *initial_state,
                                 void *out, float *final_state, kda_stream_t stream);
+
+/*
+ * Diagnostic for the failure path: launches one CTA that waits on an mbarrier
+ * no one ever arrives on, with the same bounded wait the prefill kernels use,
+ * limited to timeout_ns (0 .. 1e9).  When the limit runs out the kernel stores
+ * KDA_ERR_TIMEOUT in the device status word of desc->workspace and returns, so
+ * kda_get_device_status then reports it.  Needs only desc->workspace (at least
+ * 256 bytes); returns KDA_ERR_INVALID_ARGUMENT for a limit outside the range.
+ */
+KDA_API int kda_selftest_wait_timeout(const kda_desc *desc, int64_t timeout_ns, kda_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 KDA_API const char *kda_status_string(int status);

@@ -14,9 +14,11 @@ KDA_OK, KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA = 0, 1, 2, 3
 KDA_ERR_TIMEOUT, KDA_ERR_BAD_SEQLENS, KDA_ERR_WORKSPACE = 4, 5, 6
 KDA_F32, KDA_BF16 = 0, 1
 KDA_FLAG_CUDA_CORE_PREFILL = 1
+KDA_FLAG_SCALAR_GATE = 2
 
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_get_device_status",
-           "kda_status_string", "kda_last_cuda_error", "kda_version", "kda_prefill_noalloc")
+           "kda_status_string", "kda_last_cuda_error", "kda_version", "kda_prefill_noalloc",
+           "kda_selftest_wait_timeout")
 KDA_PREFILL_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -50,6 +52,8 @@ def _load():
     L.kda_prefill.restype = ctypes.c_int
     L.kda_prefill_noalloc.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kda_prefill_noalloc.restype = ctypes.c_int
+    L.kda_selftest_wait_timeout.argtypes = [D, ctypes.c_int64, vp]
+    L.kda_selftest_wait_timeout.restype = ctypes.c_int
     L.kda_decode_step.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kda_decode_step.restype = ctypes.c_int
     L.kda_get_device_status.argtypes = [D, vp]
@@ -133,6 +137,11 @@ def kda_prefill_noalloc(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, ini
                                    _p(cu_seqlens), _p(initial_state), _p(out), _p(final_state), _stream(stream))
 
 
+def kda_selftest_wait_timeout(desc: KdaDesc, timeout_ns: int, stream=None) -> int:
+    """Run the bounded-wait failure path on the GPU (see include/kda.h)."""
+    return lib.kda_selftest_wait_timeout(ctypes.byref(desc), int(timeout_ns), _stream(stream))
+
+
 def kda_decode_step(desc: KdaDesc, q, k, v, log_alpha, beta, state_inout, out, stream=None) -> int:
     return lib.kda_decode_step(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
                                _p(state_inout), _p(out), _stream(stream))
@@ -152,9 +161,12 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, *, ou
     """Chunk-parallel prefill (see kda_prefill in include/kda.h).
 
     Allocates ``out``, ``final_state`` and the workspace with torch when they
-    are not given.  Returns (out, final_state, workspace)."""
+    are not given.  A 2-D ``log_alpha`` [T, H] selects the scalar gate
+    (KDA_FLAG_SCALAR_GATE).  Returns (out, final_state, workspace)."""
     T, H, dk = q.shape
     dv = v.shape[2]
+    if log_alpha.dim() == 2:
+        flags |= KDA_FLAG_SCALAR_GATE
     N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     for name, t in (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta)):
         _check(t, name)
@@ -177,12 +189,13 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, *, ou
 
 
 def decode_step(q, k, v, log_alpha, beta, state, *, out=None, stream=None):
-    """One decode step, ``state`` [N,H,d_k,d_v] fp32 updated in place.  Returns out."""
+    """One decode step, ``state`` [N,H,d_k,d_v] fp32 updated in place.  A 2-D
+    ``log_alpha`` [N, H] selects the scalar gate.  Returns out."""
     N, H, dk = q.shape
     dv = v.shape[2]
     if out is None:
         out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
-    desc = make_desc(N, H, dk, dv, N, q.dtype)
+    desc = make_desc(N, H, dk, dv, N, q.dtype, flags=KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0)
     rc = kda_decode_step(desc, q, k, v, log_alpha, beta, state, out, stream)
     if rc != KDA_OK:
         raise KdaError("kda_decode_step", rc)

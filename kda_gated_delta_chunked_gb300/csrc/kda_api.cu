@@ -111,7 +111,7 @@ static Layout layout_for(const kda_desc* d) {
 static bool desc_ok(const kda_desc* d) {
     if (!d) return false;
     if (d->num_seqs < 0 || d->num_heads < 1 || d->total_tokens < 0) return false;
-    if (d->flags & ~KDA_FLAG_CUDA_CORE_PREFILL) return false;
+    if (d->flags & ~(KDA_FLAG_CUDA_CORE_PREFILL | KDA_FLAG_SCALAR_GATE)) return false;
     if (d->total_tokens > 0x7fffffffLL) return false;   // cu_seqlens is int32
     if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return false;
     if (d->d_k < 1 || d->d_v < 1) return false;
@@ -168,14 +168,17 @@ int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
     if (cu_seqlens == nullptr && N != 1) return KDA_ERR_INVALID_ARGUMENT;
     if (N == 0) return KDA_OK;
     const size_t esz = d->dtype == KDA_BF16 ? 2 : 4;
+    const bool scalar_gate = (d->flags & KDA_FLAG_SCALAR_GATE) != 0;
     const size_t nqk = (size_t)T * H * D * esz, nb = (size_t)T * H * esz;
+    const size_t nla = scalar_gate ? nb : nqk;
     const size_t nstate = (size_t)N * H * D * D * sizeof(float);
     if (T > 0) {
         if (!q || !k || !v || !log_alpha || !beta || !out) return KDA_ERR_INVALID_ARGUMENT;
-        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
+            (scalar_gate ? ((uintptr_t)log_alpha % esz) != 0 : !aligned16(log_alpha)) ||
             ((uintptr_t)beta % esz) || !aligned16(out)) return KDA_ERR_INVALID_ARGUMENT;
         const void* ins[5] = {q, k, v, log_alpha, beta};
-        const size_t szs[5] = {nqk, nqk, nqk, nqk, nb};
+        const size_t szs[5] = {nqk, nqk, nqk, nla, nb};
         for (int i = 0; i < 5; ++i)
             if (overlaps(out, nqk, ins[i], szs[i])) return KDA_ERR_INVALID_ARGUMENT;
         if (overlaps(out, nqk, initial_state, nstate) || overlaps(out, nqk, final_state, nstate))
@@ -198,7 +201,7 @@ int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
     if (e != cudaSuccess) return cuda_fail(e);
     PrefillArgs a;
     a.dtype = d->dtype; a.d = D; a.N = N; a.H = H; a.chunks_ub = (int)L.chunks_ub; a.T = T;
-    a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.beta = beta;
+    a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.beta = beta; a.la_scalar = scalar_gate ? 1 : 0;
     a.cu = cu_seqlens ? cu_seqlens : hdr->pad;
     a.s0 = initial_state; a.out = out; a.sf = final_state;
     a.hdr = hdr; a.chunk_first = chunk_first; a.recs = ws + L.rec_off; a.extra = ws + L.extra_off;
@@ -218,18 +221,21 @@ int kda_decode_step(const kda_desc* d, const void* q, const void* k, const void*
     if (N == 0) return KDA_OK;
     if (!q || !k || !v || !log_alpha || !beta || !state_inout || !out) return KDA_ERR_INVALID_ARGUMENT;
     const size_t esz = d->dtype == KDA_BF16 ? 2 : 4;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || ((uintptr_t)beta % esz) ||
+    const bool scalar_gate = (d->flags & KDA_FLAG_SCALAR_GATE) != 0;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        (scalar_gate ? ((uintptr_t)log_alpha % esz) != 0 : !aligned16(log_alpha)) || ((uintptr_t)beta % esz) ||
         ((uintptr_t)state_inout & 31u) || !aligned16(out)) return KDA_ERR_INVALID_ARGUMENT;
     if ((int64_t)N * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
     const size_t nio = (size_t)N * H * D * esz, nstate = (size_t)N * H * D * D * sizeof(float);
+    const size_t nsc = (size_t)N * H * esz;
     const void* ins[5] = {q, k, v, log_alpha, beta};
+    const size_t szs[5] = {nio, nio, nio, scalar_gate ? nsc : nio, nsc};
     for (int i = 0; i < 5; ++i)
-        if (overlaps(out, nio, ins[i], i == 4 ? (size_t)N * H * esz : nio) ||
-            overlaps(state_inout, nstate, ins[i], i == 4 ? (size_t)N * H * esz : nio))
+        if (overlaps(out, nio, ins[i], szs[i]) || overlaps(state_inout, nstate, ins[i], szs[i]))
             return KDA_ERR_INVALID_ARGUMENT;
     if (overlaps(out, nio, state_inout, nstate)) return KDA_ERR_INVALID_ARGUMENT;
-    cudaError_t e = decode_step_launch(d->dtype, D, q, k, v, log_alpha, beta, state_inout, out, N, H,
-                                       (cudaStream_t)stream);
+    cudaError_t e = decode_step_launch(d->dtype, D, q, k, v, log_alpha, scalar_gate ? 1 : 0, beta, state_inout,
+                                       out, N, H, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return KDA_OK;
 }

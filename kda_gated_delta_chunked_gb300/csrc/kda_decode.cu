@@ -4,6 +4,7 @@
 // fused recurrent KDA; recurrence of section 03, read of section 02):
 //
 //     S' = Diag(alpha) S            alpha = exp(log_alpha)      [d_k x d_v]
+//                                   (one alpha for all rows with the scalar gate)
 //     p  = S'^T k                   (what the decayed memory predicts at k)
 //     u  = beta (v - p)
 //     S  <- S' + k u^T              written back in place
@@ -51,7 +52,7 @@ __device__ __forceinline__ void st_stream_f8(float* p, const f8& x) {
 template <typename T, int D>
 __global__ void __launch_bounds__(kDecThreads)
 kda_decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                       const T* __restrict__ log_alpha, const T* __restrict__ beta,
+                       const T* __restrict__ log_alpha, int la_scalar, const T* __restrict__ beta,
                        float* __restrict__ state, T* __restrict__ out, int H) {
     constexpr int kRowsPerPass = kDecThreads / 4;   // 64
     constexpr int kPasses = D / kRowsPerPass;       // rows per thread
@@ -74,7 +75,7 @@ kda_decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
 
     const size_t vec = (size_t)nh * D;              // q, k, log_alpha, v rows of this (n, h)
     if (tid < D) {
-        sh_alpha[tid] = expf(to_f32(log_alpha[vec + tid]));
+        sh_alpha[tid] = expf(to_f32(log_alpha[la_scalar ? (size_t)nh : vec + tid]));
         sh_k[tid] = to_f32(k[vec + tid]);
         sh_q[tid] = to_f32(q[vec + tid]);
     }
@@ -146,22 +147,22 @@ kda_decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
 
 template <typename T, int D>
 static cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* la,
-                                 const void* beta, float* state, void* out, int N, int H,
+                                 int la_scalar, const void* beta, float* state, void* out, int N, int H,
                                  cudaStream_t stream) {
     dim3 grid((unsigned)N * H, D / kDecTile);
     kda_decode_step_kernel<T, D><<<grid, kDecThreads, 0, stream>>>(
-        (const T*)q, (const T*)k, (const T*)v, (const T*)la, (const T*)beta, state, (T*)out, H);
+        (const T*)q, (const T*)k, (const T*)v, (const T*)la, la_scalar, (const T*)beta, state, (T*)out, H);
     return cudaGetLastError();
 }
 
 cudaError_t decode_step_launch(int dtype, int d, const void* q, const void* k, const void* v,
-                               const void* la, const void* beta, float* state, void* out,
+                               const void* la, int la_scalar, const void* beta, float* state, void* out,
                                int N, int H, cudaStream_t stream) {
     if (dtype == KDA_BF16)
-        return d == 128 ? launch_decode<__nv_bfloat16, 128>(q, k, v, la, beta, state, out, N, H, stream)
-                        : launch_decode<__nv_bfloat16, 64>(q, k, v, la, beta, state, out, N, H, stream);
-    return d == 128 ? launch_decode<float, 128>(q, k, v, la, beta, state, out, N, H, stream)
-                    : launch_decode<float, 64>(q, k, v, la, beta, state, out, N, H, stream);
+        return d == 128 ? launch_decode<__nv_bfloat16, 128>(q, k, v, la, la_scalar, beta, state, out, N, H, stream)
+                        : launch_decode<__nv_bfloat16, 64>(q, k, v, la, la_scalar, beta, state, out, N, H, stream);
+    return d == 128 ? launch_decode<float, 128>(q, k, v, la, la_scalar, beta, state, out, N, H, stream)
+                    : launch_decode<float, 64>(q, k, v, la, la_scalar, beta, state, out, N, H, stream);
 }
 
 }  // namespace kda

@@ -21,6 +21,7 @@ struct PrefillArgs {
     int dtype, d, N, H, chunks_ub;
     int64_t T;                   // total tokens
     const void *q, *k, *v, *la, *beta;
+    int la_scalar;               // 1: la is [T, H] (one gate per token and head), else [T, H, d]
     const int32_t* cu;           // device cu_seqlens (or the workspace copy)
     const float* s0;             // initial state or nullptr
     void* out;
@@ -35,7 +36,7 @@ struct PrefillArgs {
 cudaError_t prefill_launch(int path, const PrefillArgs& a, cudaStream_t stream);
 
 cudaError_t decode_step_launch(int dtype, int d, const void* q, const void* k, const void* v,
-                               const void* la, const void* beta, float* state, void* out,
+                               const void* la, int la_scalar, const void* beta, float* state, void* out,
                                int N, int H, cudaStream_t stream);
 
 // CUDA-core (fp32) prefill.

@@ -42,7 +42,7 @@ size_t simt_record_bytes(int d) { return (5 * (size_t)kChunk * d + d) * sizeof(f
 template <typename T, int D>
 __global__ void __launch_bounds__(kSimtThreads)
 kda_simt_intra_chunk(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                     const T* __restrict__ log_alpha, const T* __restrict__ beta,
+                     const T* __restrict__ log_alpha, int la_scalar, const T* __restrict__ beta,
                      const int32_t* __restrict__ cu, const DeviceHeader* __restrict__ hdr,
                      const int32_t* __restrict__ chunk_first, int N, int H, float* __restrict__ ws) {
     if (hdr->status != KDA_OK) return;
@@ -72,7 +72,7 @@ kda_simt_intra_chunk(const T* __restrict__ q, const T* __restrict__ k, const T* 
         Ks[e] = ok ? to_f32(k[gi]) : 0.f;
         Qs[e] = ok ? to_f32(q[gi]) : 0.f;
         Vs[e] = ok ? to_f32(v[gi]) : 0.f;
-        Gs[e] = ok ? to_f32(log_alpha[gi]) : 0.f;
+        Gs[e] = ok ? to_f32(log_alpha[la_scalar ? (size_t)(t0 + r) * H + h : gi]) : 0.f;
     }
     if (tid < kChunk) bs[tid] = tid < len ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
     __syncthreads();
@@ -243,7 +243,7 @@ static cudaError_t launch_simt(const PrefillArgs& a, cudaStream_t stream) {
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[0], stream)) != cudaSuccess) return e;
     if (a.chunks_ub > 0) {
         kda_simt_intra_chunk<T, D><<<dim3(a.chunks_ub, a.H), kSimtThreads, smem_a, stream>>>(
-            (const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.la, (const T*)a.beta, a.cu,
+            (const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.la, a.la_scalar, (const T*)a.beta, a.cu,
             (const DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, (float*)a.recs);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

@@ -202,7 +202,7 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
 __global__ void __launch_bounds__(kAThreads, 2)
 kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ q,
                    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ log_alpha,
-                   const __nv_bfloat16* __restrict__ beta, const int32_t* __restrict__ cu,
+                   int la_scalar, const __nv_bfloat16* __restrict__ beta, const int32_t* __restrict__ cu,
                    DeviceHeader* __restrict__ hdr, const int32_t* __restrict__ chunk_first, int N, int H,
                    uint8_t* __restrict__ recs) {
     extern __shared__ uint8_t smem_raw[];
@@ -253,11 +253,16 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             const bool ok = r < len;
             const size_t gi = base + (size_t)r * rs;
             const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-            const uint4 la4 = ok ? *(const uint4*)(log_alpha + gi) : z4;
             kr[i] = ok ? *(const uint4*)(k + gi) : z4;
             qr[i] = ok ? *(const uint4*)(q + gi) : z4;
             float la[8];
-            unpack8(la4, la);
+            if (la_scalar) {                    // one gate per (token, head), all channels
+                const float l = ok ? __bfloat162float(log_alpha[(size_t)(t0 + r) * H + h]) : 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) la[e] = l;
+            } else {
+                unpack8(ok ? *(const uint4*)(log_alpha + gi) : z4, la);
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) { s8[e] = fmaf(la[e], kLog2e, s8[e]); gl[i][e] = s8[e]; }
         }
@@ -891,7 +896,7 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
         if (!make_v_map(&mv, a.v, T, a.H)) return cudaErrorInvalidValue;
         kda_tc_intra_chunk<<<dim3(a.chunks_ub, a.H), kAThreads, SmemA::kBytes, stream>>>(
             mv, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.la,
-            (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, (uint8_t*)a.recs);
+            a.la_scalar, (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, (uint8_t*)a.recs);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[1], stream)) != cudaSuccess) return e;

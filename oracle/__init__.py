@@ -50,6 +50,16 @@ def _f64(x) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
 
 
+def _per_channel(la: np.ndarray, dk: int) -> np.ndarray:
+    """A scalar gate (log_alpha [T, H], one per token and head: the Gated
+    DeltaNet gate, "Kimi Delta Attention" deep dive, section 03) is the
+    per-channel gate with the same value in every key channel; the C oracle
+    takes the per-channel form, so the scalar is repeated over d_k."""
+    if la.ndim == 2:
+        return np.ascontiguousarray(np.repeat(la[:, :, None], dk, axis=2))
+    return la
+
+
 def _ptr(a: Optional[np.ndarray]):
     if a is None:
         return None
@@ -89,6 +99,7 @@ class Oracle:
         q, k, v, la, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
         T, H, dk = q.shape
         dv = v.shape[2]
+        la = _per_channel(la, dk)
         if cu_seqlens is None:
             cu = np.array([0, T], dtype=np.int32)
         else:
@@ -112,6 +123,7 @@ class Oracle:
         q, k, v, la, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
         N, H, dk = q.shape
         dv = v.shape[2]
+        la = _per_channel(la, dk)
         s = _f64(state).reshape(N, H, dk, dv).copy()
         out = np.full((N, H, dv), np.nan)
         rc = self.lib.kda_oracle_decode_step(N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(la),

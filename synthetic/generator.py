@@ -106,6 +106,7 @@ class Workload:
     state_std: Optional[float] = 0.02   # None: zero initial state
     decode_seqs: int = 0            # decode workloads: sequences per step
     decode_steps: int = 0
+    gate: str = "channel"           # "channel": log_alpha [.., H, d_k]; "scalar": one per (token, head) [.., H]
 
     @property
     def total_tokens(self) -> int:
@@ -159,10 +160,15 @@ def workload(index: int) -> Workload:
 
 def custom(seed: int, seqlens, num_heads: int, d: int, dtype: str = "bf16",
            la_lo: float = 0.0005, la_hi: float = 0.1, state_std: Optional[float] = 0.02,
-           d_v: Optional[int] = None) -> Workload:
-    """A workload with the distributions of workload 1 and a caller-chosen shape."""
-    return Workload(f"custom_s{seed}", seed, num_heads, d, d if d_v is None else d_v, dtype,
-                    list(seqlens), la_lo=la_lo, la_hi=la_hi, state_std=state_std)
+           d_v: Optional[int] = None, gate: str = "channel", decode_seqs: int = 0) -> Workload:
+    """A workload with the distributions of workload 1 and a caller-chosen shape.
+    ``gate="scalar"`` draws one log_alpha per (token, head) (the Gated DeltaNet
+    gate) instead of one per key channel."""
+    if gate not in ("channel", "scalar"):
+        raise ValueError(f"gate must be 'channel' or 'scalar', not {gate!r}")
+    return Workload(f"custom_s{seed}" + ("_scalar" if gate == "scalar" else ""), seed, num_heads, d,
+                    d if d_v is None else d_v, dtype, list(seqlens), la_lo=la_lo, la_hi=la_hi,
+                    state_std=state_std, gate=gate, decode_seqs=decode_seqs)
 
 
 def _round(x64: torch.Tensor, dtype) -> torch.Tensor:
@@ -182,7 +188,10 @@ def _draw_tokens(w: Workload, stream_offset: int, t0: int, t1: int, device):
     k = normal(w.seed, st("k"), t0 * H * dk, n * H * dk, device).view(n, H, dk)
     v = normal(w.seed, st("v"), t0 * H * dv, n * H * dv, device).view(n, H, dv)
     b = normal(w.seed, st("beta"), t0 * H, n * H, device).view(n, H)
-    u = uniform(w.seed, st("log_alpha"), t0 * H * dk, n * H * dk, device).view(n, H, dk)
+    if w.gate == "scalar":
+        u = uniform(w.seed, st("log_alpha"), t0 * H, n * H, device).view(n, H)
+    else:
+        u = uniform(w.seed, st("log_alpha"), t0 * H * dk, n * H * dk, device).view(n, H, dk)
     q = _unit_rows(q) * (1.0 / math.sqrt(dk))
     k = _unit_rows(k)
     beta = torch.sigmoid(b)
@@ -214,7 +223,8 @@ def prefill_inputs(w: Workload, device="cpu", t_range=None, block_tokens: int = 
             out[name] = torch.cat(lst) if len(lst) > 1 else lst[0]
         else:
             shape = {"q": (0, w.num_heads, w.d_k), "k": (0, w.num_heads, w.d_k),
-                     "log_alpha": (0, w.num_heads, w.d_k), "v": (0, w.num_heads, w.d_v),
+                     "log_alpha": (0, w.num_heads) if w.gate == "scalar" else (0, w.num_heads, w.d_k),
+                     "v": (0, w.num_heads, w.d_v),
                      "beta": (0, w.num_heads)}[name]
             out[name] = torch.empty(shape, dtype=w.torch_dtype, device=device)
     cu = [0]

@@ -87,6 +87,38 @@ def pin_gated_deltanet(O):
         _close(sf[0, h], S, 1e-12, "GDN state")
 
 
+def pin_scalar_gate(O):
+    """A scalar gate given as log_alpha [T, H] (one per token and head) is
+    Gated DeltaNet: S_t = a_t (I - b k k^T) S_{t-1} + b k v^T, prefill and
+    decode step alike (deep dive, section 03: GDN multiplies a head's state by
+    a scalar; KDA generalises it to Diag(alpha))."""
+    rng = np.random.default_rng(RNG_SEED + 12)
+    T, H, dk, dv = 30, 3, 5, 7
+    q, k, v, la, b = _rand_case(rng, T, H, dk, dv)
+    la2 = la[:, :, 0].copy()
+    s0 = rng.standard_normal((1, H, dk, dv)) * 0.3
+    out, sf = O.prefill(q, k, v, la2, b, None, s0)
+    ref_out = np.zeros_like(out)
+    for h in range(H):
+        S = s0[0, h].copy()
+        for t in range(T):
+            kk = k[t, h]
+            S = np.exp(la2[t, h]) * (np.eye(dk) - b[t, h] * np.outer(kk, kk)) @ S + b[t, h] * np.outer(kk, v[t, h])
+            ref_out[t, h] = S.T @ q[t, h]
+        _close(sf[0, h], S, 1e-12, "scalar-gate state")
+    _close(out, ref_out, 1e-12, "scalar-gate output")
+    # one decode step with a [N, H] gate
+    st = s0[0][None].repeat(2, axis=0).reshape(2, H, dk, dv) + rng.standard_normal((2, H, dk, dv)) * 0.1
+    qd, kd, vd, lad, bd = (x[:2] for x in (q, k, v, la2, b))
+    od, sd = O.decode_step(qd, kd, vd, lad, bd, st)
+    for n in range(2):
+        for h in range(H):
+            kk = kd[n, h]
+            S = np.exp(lad[n, h]) * (np.eye(dk) - bd[n, h] * np.outer(kk, kk)) @ st[n, h] + bd[n, h] * np.outer(kk, vd[n, h])
+            _close(sd[n, h], S, 1e-12, "scalar-gate decode state")
+            _close(od[n, h], S.T @ qd[n, h], 1e-12, "scalar-gate decode output")
+
+
 def pin_no_write(O):
     """beta = 0 writes nothing: S_t = Diag(exp(sum_{s<=t} log alpha_s)) S_0 in
     closed form and o_t = S_t^T q_t; with alpha = 1 as well S stays S_0."""
@@ -279,6 +311,6 @@ def pin_zero_state_default(O):
     _close(s3, np.zeros((1, 2, 4, 3)), 0.0, "empty sequence, zero state")
 
 
-ALL_PINS = [pin_deltanet, pin_gated_deltanet, pin_no_write, pin_exact_overwrite,
+ALL_PINS = [pin_deltanet, pin_gated_deltanet, pin_scalar_gate, pin_no_write, pin_exact_overwrite,
             pin_closed_forms, pin_chunked_form, pin_continuation, pin_varlen_isolation,
             pin_mode_duality, pin_linearity, pin_exact_rational, pin_zero_state_default]

@@ -71,8 +71,8 @@ def test_prefill_host_validation():
     # unsupported head size
     bad = kda.make_desc(2, 4, 96, 96, 256, torch.bfloat16)
     assert kda.kda_prefill(bad, q, k, v, la, b, cu, s0, out, sf, 0) == kda.KDA_ERR_UNSUPPORTED
-    # flags must be 0, dtype must be known
-    bad = kda.make_desc(2, 4, 128, 128, 256, torch.bfloat16); bad.flags = 2
+    # unknown flag bits and unknown dtypes are rejected
+    bad = kda.make_desc(2, 4, 128, 128, 256, torch.bfloat16); bad.flags = 4
     assert kda.kda_prefill(bad, q, k, v, la, b, cu, s0, out, sf, 0) == kda.KDA_ERR_INVALID_ARGUMENT
     bad = kda.make_desc(2, 4, 128, 128, 256, 7)
     assert kda.kda_prefill(bad, q, k, v, la, b, cu, s0, out, sf, 0) == kda.KDA_ERR_INVALID_ARGUMENT
@@ -96,6 +96,25 @@ def test_prefill_host_validation():
     d.workspace = ws.addr + 64
     d.workspace_bytes = kda.kda_prefill_workspace_bytes(d)
     assert kda.kda_prefill(d, q, k, v, la, b, cu, s0, out, sf, 0) == kda.KDA_ERR_WORKSPACE
+
+
+def test_scalar_gate_alignment():
+    """A per-channel log_alpha needs 16-byte alignment; a scalar gate
+    ([T, H], KDA_FLAG_SCALAR_GATE) only its element size, like beta."""
+    import torch
+    q, k, v, la, b, cu, s0, out, sf, ws = _ptrs()
+    la2 = _FakePtr(la.addr + 2)
+    d = kda.make_desc(2, 4, 128, 128, 256, torch.bfloat16)
+    assert kda.kda_prefill(d, q, k, v, la2, b, cu, s0, out, sf, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    d.flags = kda.KDA_FLAG_SCALAR_GATE          # passes the pointer checks, stops at the workspace
+    assert kda.kda_prefill(d, q, k, v, la2, b, cu, s0, out, sf, 0) == kda.KDA_ERR_WORKSPACE
+    assert kda.kda_prefill(d, q, k, v, _FakePtr(la.addr + 1), b, cu, s0, out, sf, 0) == \
+        kda.KDA_ERR_INVALID_ARGUMENT
+    # the decode step: a scalar gate overlapping the state is caught with its own [N, H] size
+    q, k, v, la, b, st, o = _ptrs(n=7)
+    dd = kda.make_desc(8, 4, 128, 128, 8, torch.bfloat16, flags=kda.KDA_FLAG_SCALAR_GATE)
+    assert kda.kda_decode_step(dd, q, k, v, _FakePtr(st.addr + 62), b, st, o, 0) == \
+        kda.KDA_ERR_INVALID_ARGUMENT
 
 
 def test_decode_host_validation():
