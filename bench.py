@@ -320,6 +320,10 @@ def run_ours(args, dist: Dist):
         "clocks": clocks,
     }
 
+    # --- the same prefill with the scalar (Gated DeltaNet) gate
+    if not args.no_scalar_gate:
+        res["scalar_gate"] = bench_scalar_gate(kda, args, stream, x, s0, out, sf, ws, w)
+
     # --- decode workload (state GB/s)
     if not args.no_decode:
         res["decode"] = bench_decode(kda, args, dev, stream, peaks, peak_src)
@@ -333,6 +337,37 @@ def run_ours(args, dist: Dist):
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return res
+
+
+def bench_scalar_gate(kda, args, stream, x, s0, out, sf, ws, w):
+    """Prefill tokens/s of the same inputs with one gate per (token, head)
+    (channel 0 of log_alpha), the Gated DeltaNet form; secondary figure."""
+    T, H, D = w.total_tokens, w.num_heads, w.d_k
+    la = x["log_alpha"][:, :, 0].contiguous()
+    desc = kda.make_desc(1, H, D, D, T, w.torch_dtype, ws, flags=kda.KDA_FLAG_SCALAR_GATE)
+    steps = max(3, min(args.steps, 5))
+
+    def run():
+        rc = kda.kda_prefill(desc, x["q"], x["k"], x["v"], la, x["beta"], None, s0, out, sf, stream)
+        if rc:
+            raise kda.KdaError("kda_prefill", rc)
+
+    for _ in range(args.warmup):
+        run()
+    t0, t1 = make_events(2)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        run()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
+        raise RuntimeError("device status not OK (scalar gate)")
+    ms = t0.elapsed_time(t1) / steps
+    del la
+    return {"workload": f"{w.name}, log_alpha one per (token, head)", "value": round(T / (ms * 1e-3), 1),
+            "unit": "tokens/s", "ms_per_step": round(ms, 4), "steps": steps,
+            "gpu_launches": prefill_launches(1, H, T) * steps}
 
 
 def bench_decode(kda, args, dev, stream, peaks, peak_src):
@@ -550,6 +585,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-scalar-gate", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

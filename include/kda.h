@@ -69,7 +69,9 @@ typedef enum {
     KDA_ERR_CUDA = 3,             /* a CUDA launch or API call failed (see kda_last_cuda_error) */
     KDA_ERR_TIMEOUT = 4,          /* a bounded on-device wait gave up (device status only) */
     KDA_ERR_BAD_SEQLENS = 5,      /* cu_seqlens not 0 = c_0 <= c_1 <= ... <= c_N = T_tot (device status) */
-    KDA_ERR_WORKSPACE = 6         /* workspace missing or smaller than kda_prefill_workspace_bytes */
+    KDA_ERR_WORKSPACE = 6,        /* workspace missing or smaller than kda_prefill_workspace_bytes */
+    KDA_ERR_BAD_SNAPSHOT = 7      /* a snapshot request off its sequence, off a chunk boundary, or
+                                     repeated (device status, kda_prefill_snapshots) */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -145,6 +147,34 @@ KDA_API int kda_prefill(const kda_desc *desc,
                 void *out, float *final_state, kda_stream_t stream);
 
 /*
+ * kda_prefill that also saves the recurrent state at interior positions: the
+ * prefix checkpoints of deep dive section 07 (a cached prefix is the state
+ * after it; restoring that state and feeding the rest of the sequence
+ * continues exactly), taken in the same pass instead of one call per prefix.
+ *
+ *   num_snapshots  M >= 0 requests.
+ *   snapshot_at    int32 [M][2], device, 4-byte aligned: (sequence n, prefix
+ *                  length p) pairs, 0 <= n < N, 0 <= p <= L_n, where p is a
+ *                  multiple of 64 (the prefill's chunk size) or p = L_n.
+ *                  p = 0 gives the initial state.  No pair may repeat.
+ *   snapshots      fp32 [M, H, d_k, d_v], device, 16-byte aligned, written:
+ *                  snapshot m is the state of sequence n after its first p
+ *                  tokens (what kda_prefill over those tokens would return as
+ *                  final_state).  Must not overlap any other buffer.
+ *
+ * Every other argument is that of kda_prefill.  A request that breaks the
+ * rules above is seen on the device only: all work is skipped and the status
+ * word holds KDA_ERR_BAD_SNAPSHOT.  M = 0 is plain kda_prefill.
+ */
+KDA_API int kda_prefill_snapshots(const kda_desc *desc,
+                                  const void *q, const void *k, const void *v,
+                                  const void *log_alpha, const void *beta,
+                                  const int32_t *cu_seqlens, const float *initial_state,
+                                  void *out, float *final_state,
+                                  int32_t num_snapshots, const int32_t *snapshot_at, float *snapshots,
+                                  kda_stream_t stream);
+
+/*
  * One recurrent decode step for N independent sequences (deep dive section
  * 06, "fused recurrent KDA": decay, correct and write the state in place,
  * reading a fixed amount of memory per head).  Inputs are [N, H, *] (one
@@ -159,8 +189,9 @@ KDA_API int kda_decode_step(const kda_desc *desc,
 
 /*
  * Synchronises `stream`, then returns the device status word that the last
- * kda_prefill on this workspace recorded: KDA_OK, KDA_ERR_BAD_SEQLENS or
- * KDA_ERR_TIMEOUT (KDA_ERR_CUDA if the synchronisation itself failed).
+ * kda_prefill on this workspace recorded: KDA_OK, KDA_ERR_BAD_SEQLENS,
+ * KDA_ERR_BAD_SNAPSHOT or KDA_ERR_TIMEOUT (KDA_ERR_CUDA if the
+ * synchronisation itself failed).
  */
 KDA_API int kda_get_device_status(const kda_desc *desc, kda_stream_t stream);
 

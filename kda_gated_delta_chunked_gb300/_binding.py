@@ -11,14 +11,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.environ.get("KDA_LIBRARY", os.path.join(_HERE, "_build", "libkda.so"))
 
 KDA_OK, KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA = 0, 1, 2, 3
-KDA_ERR_TIMEOUT, KDA_ERR_BAD_SEQLENS, KDA_ERR_WORKSPACE = 4, 5, 6
+KDA_ERR_TIMEOUT, KDA_ERR_BAD_SEQLENS, KDA_ERR_WORKSPACE, KDA_ERR_BAD_SNAPSHOT = 4, 5, 6, 7
 KDA_F32, KDA_BF16 = 0, 1
 KDA_FLAG_CUDA_CORE_PREFILL = 1
 KDA_FLAG_SCALAR_GATE = 2
 
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_get_device_status",
            "kda_status_string", "kda_last_cuda_error", "kda_version", "kda_prefill_noalloc",
-           "kda_selftest_wait_timeout")
+           "kda_selftest_wait_timeout", "kda_prefill_snapshots")
 KDA_PREFILL_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -50,6 +50,8 @@ def _load():
     L.kda_prefill_workspace_bytes.restype = ctypes.c_size_t
     L.kda_prefill.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kda_prefill.restype = ctypes.c_int
+    L.kda_prefill_snapshots.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp]
+    L.kda_prefill_snapshots.restype = ctypes.c_int
     L.kda_prefill_noalloc.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kda_prefill_noalloc.restype = ctypes.c_int
     L.kda_selftest_wait_timeout.argtypes = [D, ctypes.c_int64, vp]
@@ -130,6 +132,14 @@ def kda_prefill(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, initial_sta
                            _p(cu_seqlens), _p(initial_state), _p(out), _p(final_state), _stream(stream))
 
 
+def kda_prefill_snapshots(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state,
+                          num_snapshots: int, snapshot_at, snapshots, stream=None) -> int:
+    """Raw C call of the prefill with state snapshots (see include/kda.h)."""
+    return lib.kda_prefill_snapshots(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
+                                     _p(cu_seqlens), _p(initial_state), _p(out), _p(final_state),
+                                     int(num_snapshots), _p(snapshot_at), _p(snapshots), _stream(stream))
+
+
 def kda_prefill_noalloc(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state,
                         stream=None) -> int:
     """Raw C call of the no-workspace prefill (the library's fixed scratch area)."""
@@ -157,12 +167,19 @@ def _check(t: torch.Tensor, name: str):
 
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, *, out=None,
-            final_state=None, workspace=None, stream=None, want_final_state: bool = True, flags: int = 0):
+            final_state=None, workspace=None, stream=None, want_final_state: bool = True, flags: int = 0,
+            snapshot_at=None, snapshots=None):
     """Chunk-parallel prefill (see kda_prefill in include/kda.h).
 
     Allocates ``out``, ``final_state`` and the workspace with torch when they
     are not given.  A 2-D ``log_alpha`` [T, H] selects the scalar gate
-    (KDA_FLAG_SCALAR_GATE).  Returns (out, final_state, workspace)."""
+    (KDA_FLAG_SCALAR_GATE).  Returns (out, final_state, workspace).
+
+    ``snapshot_at`` (int32 [M, 2] CUDA tensor of (sequence, prefix length)
+    pairs) also saves the state after each of those prefixes into
+    ``snapshots`` [M, H, d_k, d_v] (allocated if not given) through
+    kda_prefill_snapshots; the call then returns (out, final_state, workspace,
+    snapshots)."""
     T, H, dk = q.shape
     dv = v.shape[2]
     if log_alpha.dim() == 2:
@@ -182,10 +199,22 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, *, ou
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     desc.workspace = workspace.data_ptr()
     desc.workspace_bytes = workspace.numel()
-    rc = kda_prefill(desc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state, stream)
+    if snapshot_at is None:
+        rc = kda_prefill(desc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state, stream)
+        if rc != KDA_OK:
+            raise KdaError("kda_prefill", rc)
+        return out, final_state, workspace
+    _check(snapshot_at, "snapshot_at")
+    if snapshot_at.dtype != torch.int32 or snapshot_at.dim() != 2 or snapshot_at.shape[1] != 2:
+        raise ValueError("snapshot_at must be an int32 [M, 2] tensor of (sequence, prefix length)")
+    M = snapshot_at.shape[0]
+    if snapshots is None:
+        snapshots = torch.empty((M, H, dk, dv), dtype=torch.float32, device=q.device)
+    rc = kda_prefill_snapshots(desc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state,
+                               M, snapshot_at, snapshots, stream)
     if rc != KDA_OK:
-        raise KdaError("kda_prefill", rc)
-    return out, final_state, workspace
+        raise KdaError("kda_prefill_snapshots", rc)
+    return out, final_state, workspace, snapshots
 
 
 def decode_step(q, k, v, log_alpha, beta, state, *, out=None, stream=None):

@@ -82,6 +82,40 @@ kda_sequence_table(const int32_t* __restrict__ cu_in, int N, int64_t T_tot, Devi
 }
 
 // ---------------------------------------------------------------------------
+// Snapshot requests: one CTA per request (sequence n, prefix length p).  A
+// request at p = 0 copies the initial state; any other marks the chunk that
+// ends at p, whose state the inter-chunk kernels write out after processing
+// it.  Checks every request; a bad or repeated one sets KDA_ERR_BAD_SNAPSHOT.
+// slot[] holds -1 on entry (set by the caller's memset).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+kda_snapshot_table(const int32_t* __restrict__ at, const int32_t* __restrict__ cu, const int32_t* chunk_first,
+                   int N, int H, int D, DeviceHeader* hdr, int32_t* slot, const float* __restrict__ s0,
+                   float* __restrict__ snaps) {
+    if (hdr->status != KDA_OK) return;
+    const int m = blockIdx.x;
+    const int n = at[2 * m], p = at[2 * m + 1];
+    if (n < 0 || n >= N) { if (threadIdx.x == 0) record_status(hdr, KDA_ERR_BAD_SNAPSHOT); return; }
+    const int len = cu[n + 1] - cu[n];
+    if (p < 0 || p > len || (p % kChunk != 0 && p != len)) {
+        if (threadIdx.x == 0) record_status(hdr, KDA_ERR_BAD_SNAPSHOT);
+        return;
+    }
+    if (p == 0) {                                  // the state before any token
+        const size_t per = (size_t)H * D * D;
+        float4* dst = (float4*)(snaps + (size_t)m * per);
+        const float4* src = s0 ? (const float4*)(s0 + (size_t)n * per) : nullptr;
+        for (size_t e = threadIdx.x; e < per / 4; e += blockDim.x)
+            dst[e] = src ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        const int c = chunk_first[n] + (p + kChunk - 1) / kChunk - 1;
+        if (atomicCAS(&slot[c], -1, m) != -1) record_status(hdr, KDA_ERR_BAD_SNAPSHOT);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Workspace layout
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -90,6 +124,7 @@ struct Layout {
     int path;              // which prefill path runs
     int64_t chunks_ub;     // upper bound on total chunks: ceil(T/C) + N
     size_t table_off;      // int32 chunk_first[N+1]
+    size_t slot_off;       // int32 snapshot slot per chunk [chunks_ub]
     size_t rec_off;        // per-(chunk, head) records
     size_t rec_bytes;
     size_t extra_off;      // path-specific scratch
@@ -101,7 +136,8 @@ static Layout layout_for(const kda_desc* d) {
     L.path = choose_prefill_path(d->dtype, d->d_k, d->flags);
     L.chunks_ub = (d->total_tokens + kChunk - 1) / kChunk + d->num_seqs;
     L.table_off = sizeof(DeviceHeader);
-    L.rec_off = align_up(L.table_off + ((size_t)d->num_seqs + 1) * sizeof(int32_t), 1024);
+    L.slot_off = align_up(L.table_off + ((size_t)d->num_seqs + 1) * sizeof(int32_t), 256);
+    L.rec_off = align_up(L.slot_off + (size_t)L.chunks_ub * sizeof(int32_t), 1024);
     L.rec_bytes = prefill_record_bytes(L.path, d->d_k);
     L.extra_off = align_up(L.rec_off + (size_t)L.chunks_ub * d->num_heads * L.rec_bytes, 1024);
     L.total = L.extra_off + prefill_extra_bytes(L.path, d->num_seqs, d->num_heads, d->total_tokens);
@@ -149,6 +185,7 @@ const char* kda_status_string(int s) {
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
         case KDA_ERR_BAD_SEQLENS: return "KDA_ERR_BAD_SEQLENS";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_BAD_SNAPSHOT: return "KDA_ERR_BAD_SNAPSHOT";
         default: return "KDA_ERR_UNKNOWN";
     }
 }
@@ -158,9 +195,10 @@ size_t kda_prefill_workspace_bytes(const kda_desc* d) {
     return layout_for(d).total;
 }
 
-int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
-                const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
-                const float* initial_state, void* out, float* final_state, kda_stream_t stream) {
+static int prefill_impl(const kda_desc* d, const void* q, const void* k, const void* v,
+                        const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
+                        const float* initial_state, void* out, float* final_state, int32_t num_snaps,
+                        const int32_t* snap_at, float* snaps, kda_stream_t stream) {
     if (!desc_ok(d)) return KDA_ERR_INVALID_ARGUMENT;
     if (!shape_supported(d)) return KDA_ERR_UNSUPPORTED;
     const int N = d->num_seqs, H = d->num_heads, D = d->d_k;
@@ -188,6 +226,16 @@ int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
         (final_state && !aligned16(final_state))) return KDA_ERR_INVALID_ARGUMENT;
     if (initial_state && final_state && initial_state != (const float*)final_state &&
         overlaps(initial_state, nstate, final_state, nstate)) return KDA_ERR_INVALID_ARGUMENT;
+    if (num_snaps < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (num_snaps > 0) {
+        if (!snap_at || !snaps || ((uintptr_t)snap_at & 3u) || !aligned16(snaps)) return KDA_ERR_INVALID_ARGUMENT;
+        const size_t nsnap = (size_t)num_snaps * H * D * D * sizeof(float);
+        const size_t nat = (size_t)num_snaps * 2 * sizeof(int32_t);
+        const void* bufs[9] = {q, k, v, log_alpha, beta, out, initial_state, final_state, snap_at};
+        const size_t szs[9] = {nqk, nqk, nqk, nla, nb, nqk, nstate, nstate, nat};
+        for (int i = 0; i < 9; ++i)
+            if (overlaps(snaps, nsnap, bufs[i], szs[i])) return KDA_ERR_INVALID_ARGUMENT;
+    }
     const Layout L = layout_for(d);
     if (!d->workspace || d->workspace_bytes < L.total || ((uintptr_t)d->workspace & 255u))
         return KDA_ERR_WORKSPACE;
@@ -199,6 +247,14 @@ int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
     kda_sequence_table<<<1, kPrepThreads, 0, s>>>(cu_seqlens, N, T, hdr, chunk_first, L.chunks_ub);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
+    int32_t* slot = (int32_t*)(ws + L.slot_off);
+    if (num_snaps > 0) {
+        if ((e = cudaMemsetAsync(slot, 0xff, (size_t)L.chunks_ub * sizeof(int32_t), s)) != cudaSuccess)
+            return cuda_fail(e);
+        kda_snapshot_table<<<num_snaps, 256, 0, s>>>(snap_at, cu_seqlens ? cu_seqlens : hdr->pad, chunk_first, N, H,
+                                                     D, hdr, slot, initial_state, snaps);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    }
     PrefillArgs a;
     a.dtype = d->dtype; a.d = D; a.N = N; a.H = H; a.chunks_ub = (int)L.chunks_ub; a.T = T;
     a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.beta = beta; a.la_scalar = scalar_gate ? 1 : 0;
@@ -206,9 +262,26 @@ int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
     a.s0 = initial_state; a.out = out; a.sf = final_state;
     a.hdr = hdr; a.chunk_first = chunk_first; a.recs = ws + L.rec_off; a.extra = ws + L.extra_off;
     a.phase_events = (cudaEvent_t*)d->phase_events;
+    a.snap_slot = num_snaps > 0 ? slot : nullptr;
+    a.snaps = num_snaps > 0 ? snaps : nullptr;
     e = prefill_launch(L.path, a, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return KDA_OK;
+}
+
+int kda_prefill(const kda_desc* d, const void* q, const void* k, const void* v,
+                const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
+                const float* initial_state, void* out, float* final_state, kda_stream_t stream) {
+    return prefill_impl(d, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state, 0, nullptr,
+                             nullptr, stream);
+}
+
+int kda_prefill_snapshots(const kda_desc* d, const void* q, const void* k, const void* v,
+                          const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
+                          const float* initial_state, void* out, float* final_state, int32_t num_snapshots,
+                          const int32_t* snapshot_at, float* snapshots, kda_stream_t stream) {
+    return prefill_impl(d, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state,
+                             num_snapshots, snapshot_at, snapshots, stream);
 }
 
 int kda_decode_step(const kda_desc* d, const void* q, const void* k, const void* v,

@@ -31,6 +31,8 @@ struct PrefillArgs {
     void* recs;                  // per-(chunk, head) records
     void* extra;                 // path-specific scratch after the records
     cudaEvent_t* phase_events;   // optional timing events (3) or nullptr
+    const int32_t* snap_slot;    // [chunks] snapshot index to write after each chunk (-1: none), or nullptr
+    float* snaps;                // snapshot states [M, H, d, d] (with snap_slot)
 };
 
 cudaError_t prefill_launch(int path, const PrefillArgs& a, cudaStream_t stream);

@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(kSimtThreads)
 kda_simt_inter_chunk(const int32_t* __restrict__ cu, const DeviceHeader* __restrict__ hdr,
                      const int32_t* __restrict__ chunk_first, int H,
                      const float* __restrict__ ws, const float* __restrict__ initial_state,
-                     T* __restrict__ out, float* __restrict__ final_state) {
+                     T* __restrict__ out, float* __restrict__ final_state,
+                     const int32_t* __restrict__ snap_slot, float* __restrict__ snaps) {
     if (hdr->status != KDA_OK) return;
     const int nh = blockIdx.x;
     const int n = nh / H, h = nh % H;
@@ -215,11 +216,14 @@ kda_simt_inter_chunk(const int32_t* __restrict__ cu, const DeviceHeader* __restr
                     from_f32<T>(rec[SimtRec<D>::kO0 + (size_t)i * D + col0 + j] + qs_);
         }
         __syncthreads();
-        // S <- Diag(Gamma) S + K^end^T U.
+        // S <- Diag(Gamma) S + K^end^T U; written out too if a snapshot is
+        // requested after this chunk.
+        const int snap_m = snap_slot ? snap_slot[c] : -1;
         for (int ch = r0; ch < D; ch += kSimtThreads / kSimtTile) {
             float acc = Gsm[ch] * Ssm[ch * kSimtTile + j];
             for (int i = 0; i < kChunk; ++i) acc += Esm[i * D + ch] * Usm[i * kSimtTile + j];
             Ssm[ch * kSimtTile + j] = acc;
+            if (snap_m >= 0) snaps[(((size_t)snap_m * H + h) * D + ch) * D + col0 + j] = acc;
         }
     }
     __syncthreads();
@@ -249,7 +253,8 @@ static cudaError_t launch_simt(const PrefillArgs& a, cudaStream_t stream) {
     }
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[1], stream)) != cudaSuccess) return e;
     kda_simt_inter_chunk<T, D><<<dim3((unsigned)a.N * a.H, D / kSimtTile), kSimtThreads, smem_b, stream>>>(
-        a.cu, (const DeviceHeader*)a.hdr, a.chunk_first, a.H, (const float*)a.recs, a.s0, (T*)a.out, a.sf);
+        a.cu, (const DeviceHeader*)a.hdr, a.chunk_first, a.H, (const float*)a.recs, a.s0, (T*)a.out, a.sf,
+        a.snap_slot, a.snaps);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[2], stream)) != cudaSuccess) return e;
     return cudaSuccess;

@@ -31,10 +31,13 @@
 //   3. With A^[i][j] = beta_j (K~ K^T)[i][j] (j < i), the rows of
 //      Y^ = [T; P T] solve  Y^ (I + A^) = [Diag(beta); P Diag(beta)]  (beta
 //      folded into the columns, so the solution needs no later rescaling).
-//      The solve runs in 16-column blocks from the right: the coupling to the
-//      already solved blocks is one small MMA (M=128, N=16) from the bf16 Y^
-//      and A^ (stored row by row, read MN-major), the 16 x 16 diagonal block a
-//      short fp32 recursion.
+//      The solve runs in 16-column blocks from the right.  The inverses E_J
+//      of the four 16 x 16 diagonal blocks are formed first (fp32 forward
+//      substitution, one thread per column), then in parallel the blocks'
+//      right-hand sides times E_J and the coupling blocks A^_KJ E_J; what
+//      remains sequential is one small MMA per block (M=128, N=16, from the
+//      bf16 Y^ and the coupling blocks stored row by row, read MN-major) and a
+//      subtraction.
 //   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~m | V] with K~m read MN-major
 //      from the MMA-a operand; since K~ = K~m Diag(2^g_m), W, P T K~ and Q~
 //      are rescaled per channel in the epilogue, Q' = Q~ - P T K~.
@@ -47,14 +50,17 @@
 // channel sums and stored to TMEM where MMA-a would have put them, and the
 // reference point moves to the chunk start (g_m = 0).
 //
-// Kernel (b), one CTA per (sequence, head, 16-column tile of the state):
-// a producer warp streams each chunk's record into a 3-stage shared-memory
-// ring with 1-D bulk copies; four consumer warps keep their 128 x 16 slice of
-// S in fp32 registers (thread i = key channel i) and per chunk issue
-//   MMA1 (M=128, N=16, K=128): [W; Q'] S  -> U = U0 - W S (rows 0..63),
+// Kernel (b), one CTA per (sequence, head, segment of chunks), 16 consumer
+// warps and a producer warp: the producer streams each chunk's record into a
+// two-stage shared-memory ring with 1-D bulk copies; the consumers keep the
+// whole 128 x 128 state of the head in fp32 registers (one row and 32 columns
+// per thread) and per chunk one thread issues
+//   MMA1 (M=128, N=128, K=128): [W; Q'] S  -> U = U0 - W S (rows 0..63),
 //                                             O = O0 + Q' S (rows 64..127)
-//   MMA3 (M=128, N=16, K=64):  K^end^T U  -> S <- Gamma * S + K^end^T U
-// with S and U fed back to the tensor core as bf16 MN-major operands.
+//   MMA3 (M=128, N=128, K=64):  K^end^T U  -> S <- Gamma * S + K^end^T U
+// with S and U fed back to the tensor core as bf16 MN-major operands.  Long
+// sequences are cut into segments that run in parallel (see the segment scan
+// below the kernel (a) code).
 //
 // Every wait on an mbarrier is bounded; on timeout the kernel records
 // KDA_ERR_TIMEOUT in the device status word, drains its own copies and exits.
@@ -69,8 +75,7 @@ namespace kda {
 using namespace sm100;
 
 constexpr int kTcD = 128;                // head size handled here
-constexpr int kTile = 16;                // state columns per CTA of kernel (b)
-constexpr int kTiles = kTcD / kTile;
+constexpr int kTile = 16;                // columns per tile of the U0 / O0 record images
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxSpanLog2 = 100.f;    // fast path if max_c (g_0 - g_C) <= 100 (log2 units)
@@ -107,6 +112,7 @@ struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per 
     static constexpr uint32_t kOpB1 = 49152;    // MMA-a B K^m, K-major, 2 K-blocks x 8 KB; then:
     static constexpr uint32_t kAt = 49152;      //   A^ by 16-column blocks, MN-major 32B-swizzle, 4 x 2 KB
     static constexpr uint32_t kAt32 = 57344;    //   diagonal 16 x 16 blocks of A^ transposed, fp32, 4 KB
+    static constexpr uint32_t kE32 = 61440;     //   E_J = (I + A^_JJ)^-1 of the diagonal blocks, fp32, 4 KB
     static constexpr uint32_t kY = 65536;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB
     static constexpr uint32_t kPart = 65536;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
     static constexpr uint32_t kGS = 49152;      // (slow path, before A^) g, fp32 [64][128], 32 KB
@@ -130,18 +136,52 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                       pack_bf16x2(f[6], f[7]));
 }
 
-// Column block J (16 columns) of the solve Y^ (I + A^) = RHS for row `tid`
-// (threads 0..127) of Y^: the right-hand side (from the Gram / Q~ K^T
-// accumulator still in TMEM columns 0..63), minus the coupling to the solved
-// blocks on the right (one MMA from the bf16 Y^ and A^ into TMEM columns
-// 64..79), then the in-block recursion on the fp32 diagonal block; stored to
-// Y^ as bf16.  Threads 128..255 only take part in the barrier.
+// The solve Y^ (I + A^) = RHS, RHS = [Diag(beta); P Diag(beta)], by 16-column
+// blocks J = 3..0.  With D_J = I + A^_JJ (unit lower triangular) and
+// E_J = D_J^-1, block J of the solution is
+//     Y^_J = RHS_J E_J - sum_{K>J} Y^_K (A^_KJ E_J),
+// so once the four E_J, the right-hand sides R'_J = RHS_J E_J and the coupling
+// blocks M_KJ = A^_KJ E_J are formed (all independent of Y^, computed in
+// parallel), the sequential part is one small MMA per block (Y^_K M_KJ into
+// TMEM columns 64..79) and a subtraction: no recursion on the critical path.
+
+// y[c] = sum_{l >= c} r[l] E[l][c] for one 16-wide row r and E = E_J (fp32,
+// row-major [16][16] in shared memory, lower triangular).
+__device__ __forceinline__ void row_times_e(const float (&r)[16], const float* E, float (&y)[16]) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) y[c] = 0.f;
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+        const float4* e4 = (const float4*)(E + 16 * l);
+#pragma unroll
+        for (int g = 0; g <= (l >> 2); ++g) {
+            const float4 e = e4[g];
+            if (4 * g + 0 <= l) y[4 * g + 0] = fmaf(r[l], e.x, y[4 * g + 0]);
+            if (4 * g + 1 <= l) y[4 * g + 1] = fmaf(r[l], e.y, y[4 * g + 1]);
+            if (4 * g + 2 <= l) y[4 * g + 2] = fmaf(r[l], e.z, y[4 * g + 2]);
+            if (4 * g + 3 <= l) y[4 * g + 3] = fmaf(r[l], e.w, y[4 * g + 3]);
+        }
+    }
+}
+
+// Stores 16 values as bf16 into columns 16J..16J+15 of row `row` of Y^.
+__device__ __forceinline__ void store_y16(uint8_t* yop, int row, int J, const float (&y)[16]) {
+    float lo[8], hi[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) { lo[e] = y[e]; hi[e] = y[8 + e]; }
+    *(uint4*)(yop + sw128_off(row, 16 * J)) = pack8(lo);
+    *(uint4*)(yop + sw128_off(row, 16 * J + 8)) = pack8(hi);
+}
+
+// Block J < 3 of the sequential part: the coupling MMA, then Y^_J = R'_J - it.
+// Rows 0..63 are finished by warps 0,1 (R' nonzero only in the row's own
+// block), rows 64..127 by the two warps of lane quarters 2,3 that hold R'_J.
 template <int J>
-__device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const float* s_beta, uint64_t* bar,
-                                          int* s_flag, uint32_t& mph, bool& abort) {
-    const int tid = threadIdx.x, warp = tid >> 5;
+__device__ __forceinline__ void solve_block(uint8_t* sm, uint32_t tmem, uint64_t* bar, int* s_flag, uint32_t& mph,
+                                            bool& abort, const float (&y0)[16], const float (&yP)[2][16]) {
+    const int tid = threadIdx.x, warp = tid >> 5, quarter = warp & 3;
     uint8_t* yop = sm + SmemA::kY;
-    if (J < 3 && tid == 0 && !abort) {
+    if (tid == 0 && !abort) {
 #pragma unroll
         for (int ks = J + 1; ks < 4; ++ks)
             mma_bf16_ss(tmem + 64, sdesc_k_sw128(smem_u32(yop + ks * 32)),
@@ -149,60 +189,38 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
                         idesc_bf16(128, 16, 0, 1), ks > J + 1);
         mma_commit(bar);
     }
-    if (warp < 4) {
-        const float4* at32v = (const float4*)(sm + SmemA::kAt32);
-        float z[16];
-        if (warp < 2) {
+    const bool top = warp < 2;
+    const bool bottom = quarter >= 2 && ((warp < 4) == (J >= 2));
+    if (top || bottom) {
+        if (!abort && !mbar_wait(bar, mph & 1, kWaitNs)) s_flag[1] = 1;
+        tc_fence_after_sync();
+        float d[16], y[16];
+        tmem_ld16(tmem_addr(tmem, 32 * quarter, 64), d);
+        tmem_wait_ld();
+        if (top) {
+            const bool own = (tid >> 4) == J;          // row tid lies in block J
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) z[jj] = (16 * J + jj == tid) ? s_beta[tid] : 0.f;
+            for (int c = 0; c < 16; ++c) y[c] = (own ? y0[c] : 0.f) - d[c];
+            store_y16(yop, tid, J, y);
         } else {
-            const int i = tid - 64;
-            float f[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * J), f);
-            tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) z[jj] = (16 * J + jj <= i) ? f[jj] * s_beta[16 * J + jj] : 0.f;
+            for (int c = 0; c < 16; ++c) y[c] = yP[J & 1][c] - d[c];
+            store_y16(yop, 64 + (quarter & 1) * 32 + (tid & 31), J, y);
         }
-        if (J < 3) {
-            if (!abort && !mbar_wait(bar, mph & 1, kWaitNs)) s_flag[1] = 1;
-            tc_fence_after_sync();
-            float dd[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 64), dd);
-            tmem_wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) z[jj] -= dd[jj];
-        }
-#pragma unroll
-        for (int jj = 14; jj >= 0; --jj) {
-            float acc = z[jj];
-#pragma unroll
-            for (int g4 = (jj + 1) >> 2; g4 < 4; ++g4) {
-                const float4 a = at32v[(J * 16 + jj) * 4 + g4];
-                if (4 * g4 + 0 > jj) acc = fmaf(-z[4 * g4 + 0], a.x, acc);
-                if (4 * g4 + 1 > jj) acc = fmaf(-z[4 * g4 + 1], a.y, acc);
-                if (4 * g4 + 2 > jj) acc = fmaf(-z[4 * g4 + 2], a.z, acc);
-                if (4 * g4 + 3 > jj) acc = fmaf(-z[4 * g4 + 3], a.w, acc);
-            }
-            z[jj] = acc;
-        }
-        uint32_t p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) p[e] = pack_bf16x2(z[2 * e], z[2 * e + 1]);
-        *(uint4*)(yop + sw128_off(tid, 16 * J)) = make_uint4(p[0], p[1], p[2], p[3]);
-        *(uint4*)(yop + sw128_off(tid, 16 * J + 8)) = make_uint4(p[4], p[5], p[6], p[7]);
         fence_proxy_async_smem();
     }
-    if (J < 3) ++mph;
+    ++mph;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     abort = s_flag[1] != 0;
 }
 
+template <bool kScalarGate>
 __global__ void __launch_bounds__(kAThreads, 2)
 kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ q,
                    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ log_alpha,
-                   int la_scalar, const __nv_bfloat16* __restrict__ beta, const int32_t* __restrict__ cu,
+                   const __nv_bfloat16* __restrict__ beta, const int32_t* __restrict__ cu,
                    DeviceHeader* __restrict__ hdr, const int32_t* __restrict__ chunk_first, int N, int H,
                    uint8_t* __restrict__ recs) {
     extern __shared__ uint8_t smem_raw[];
@@ -214,12 +232,17 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     int* s_flag = (int*)(sm + SmemA::kMisc + 816);                // [0] slow path, [1] abort
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (hdr->status != KDA_OK) return;
     const int c = blockIdx.x, h = blockIdx.y;
-    if (c >= hdr->total_chunks) return;
-    const int n = chunk_owner(chunk_first, N, c);
-    const int64_t t0 = (int64_t)cu[n] + (int64_t)(c - chunk_first[n]) * kChunk;
-    const int len = (int)min64(kChunk, (int64_t)cu[n + 1] - t0);
+    // The status word, the chunk's sequence and its bounds are loaded together
+    // (one memory round trip for a single sequence); the tables are always
+    // written, so reading them before the status check is safe.
+    const int status = hdr->status, total_chunks = hdr->total_chunks;
+    const int n = N == 1 ? 0 : chunk_owner(chunk_first, N, c);
+    const int64_t seq_begin = cu[n], seq_end = cu[n + 1];
+    const int c_first = chunk_first[n];
+    if (status != KDA_OK || c >= total_chunks) return;
+    const int64_t t0 = seq_begin + (int64_t)(c - c_first) * kChunk;
+    const int len = (int)min64(kChunk, seq_end - t0);
     uint8_t* rec = recs + ((size_t)c * H + h) * TcRec::kBytes;
 
     if (tid == 0) {
@@ -256,7 +279,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             kr[i] = ok ? *(const uint4*)(k + gi) : z4;
             qr[i] = ok ? *(const uint4*)(q + gi) : z4;
             float la[8];
-            if (la_scalar) {                    // one gate per (token, head), all channels
+            if (kScalarGate) {                  // one gate per (token, head), all channels
                 const float l = ok ? __bfloat162float(log_alpha[(size_t)(t0 + r) * H + h]) : 0.f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) la[e] = l;
@@ -442,10 +465,113 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     tc_fence_after_sync();
 
     // ---- Y^ (I + A^) = [Diag(beta); P Diag(beta)], 16-column blocks from the right.
-    inv_block<3>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
-    inv_block<2>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
-    inv_block<1>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
-    inv_block<0>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
+    {
+        const int quarter = warp & 3;
+        float* e32 = (float*)(sm + SmemA::kE32);
+        float y0[16], yP[2][16];
+        // (i) rows 64..127 of the right-hand side, P Diag(beta) (P = Q~ K^T,
+        // j <= i): lane quarters 2,3; warps 2,3 take blocks 2,3, warps 6,7 blocks 0,1.
+        if (quarter >= 2) {
+            const int jb = warp < 4 ? 2 : 0, i = (quarter & 1) * 32 + lane;
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, 16 * jb), yP[0]);
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, 16 * jb + 16), yP[1]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int j = 16 * (jb + b) + c;
+                    yP[b][c] = j <= i ? yP[b][c] * s_beta[j] : 0.f;
+                }
+        }
+        // (ii) E_J = (I + L)^-1, L = A^_JJ strictly lower: column c of E by
+        // forward substitution, E[l][c] = delta_lc - sum_{m<l} L[l][m] E[m][c],
+        // in right-looking order (once E[m][c] is final it updates every later
+        // row), so the dependent chain is one FMA per row.
+        if (tid < 64) {
+            const int J = tid >> 4, c = tid & 15;
+            const float4* at4 = (const float4*)(sm + SmemA::kAt32) + J * 64;   // column m of L: at4[4m .. 4m+3]
+            float e[16];
+#pragma unroll
+            for (int l = 0; l < 16; ++l) e[l] = l == c ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < 15; ++m) {
+                float lc[16];
+#pragma unroll
+                for (int g = (m + 1) >> 2; g < 4; ++g) {
+                    const float4 v = at4[4 * m + g];
+                    lc[4 * g] = v.x; lc[4 * g + 1] = v.y; lc[4 * g + 2] = v.z; lc[4 * g + 3] = v.w;
+                }
+#pragma unroll
+                for (int l = m + 1; l < 16; ++l) e[l] = fmaf(-lc[l], e[m], e[l]);
+            }
+#pragma unroll
+            for (int l = 0; l < 16; ++l) e32[(16 * J + l) * 16 + c] = e[l];
+        }
+        __syncthreads();
+        // (iii) R'_J = RHS_J E_J.  Rows 0..63: RHS = Diag(beta), so row i is
+        // beta_i times row (i mod 16) of E_{i/16} (zero in the other blocks).
+        if (quarter >= 2) {
+            const int jb = warp < 4 ? 2 : 0;
+            float r[16];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) r[c] = yP[b][c];
+                row_times_e(r, e32 + (jb + b) * 256, yP[b]);
+            }
+        } else if (warp < 2) {
+            const float bi = s_beta[tid];
+            const float4* e4 = (const float4*)(e32 + (tid >> 4) * 256 + (tid & 15) * 16);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 e = e4[g];
+                y0[4 * g] = bi * e.x; y0[4 * g + 1] = bi * e.y; y0[4 * g + 2] = bi * e.z; y0[4 * g + 3] = bi * e.w;
+            }
+        }
+        // (iv) coupling blocks M_KJ = A^_KJ E_J (K > J), in place of A^_KJ in the
+        // bf16 MN-major blocks the coupling MMAs read: warps 0,1,4, one row each.
+        if (warp < 2 || warp == 4) {
+            const int u = warp < 2 ? tid : tid - 64;          // 0..95
+            const int pair = u >> 4, a = u & 15;
+            const int K = pair < 3 ? pair + 1 : (pair < 5 ? pair - 1 : 3);
+            const int J = pair < 3 ? 0 : (pair < 5 ? 1 : 2);
+            uint8_t* blk = sm + SmemA::kAt + J * 2048;
+            const int row = 16 * K + a;
+            float r[16], m[16];
+            {
+                float lo[8], hi[8];
+                unpack8(*(const uint4*)(blk + sw32_off(row, 0)), lo);
+                unpack8(*(const uint4*)(blk + sw32_off(row, 8)), hi);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { r[e] = lo[e]; r[8 + e] = hi[e]; }
+            }
+            row_times_e(r, e32 + J * 256, m);
+            float lo[8], hi[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { lo[e] = m[e]; hi[e] = m[8 + e]; }
+            *(uint4*)(blk + sw32_off(row, 0)) = pack8(lo);
+            *(uint4*)(blk + sw32_off(row, 8)) = pack8(hi);
+        }
+        // (v) block 3 has nothing on its right: Y^_3 = R'_3.
+        if (warp < 2) {
+            float y[16];
+            const bool own = (tid >> 4) == 3;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) y[c] = own ? y0[c] : 0.f;
+            store_y16(sm + SmemA::kY, tid, 3, y);
+        } else if (warp == 2 || warp == 3) {
+            store_y16(sm + SmemA::kY, 64 + (quarter & 1) * 32 + lane, 3, yP[1]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        abort = s_flag[1] != 0;
+        solve_block<2>(sm, tmem, &bars[1], s_flag, mph, abort, y0, yP);
+        solve_block<1>(sm, tmem, &bars[1], s_flag, mph, abort, y0, yP);
+        solve_block<0>(sm, tmem, &bars[1], s_flag, mph, abort, y0, yP);
+    }
 
     // ---- MMA-b: Y^ [K~m | V] -> [[W Em^-1, U0], [P T K~m, O0]].  Its issuing
     // thread waits for the V tile first (the MMA reads it).
@@ -479,10 +605,15 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         uint8_t* a1 = rec + TcRec::kA1;
         const uint8_t* qm = sm + SmemA::kOpA;
 #pragma unroll 1
-        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
-            float f[16];
-            tmem_ld16(tmem_addr(tmem, 32 * quarter, c0), f);
-            tmem_wait_ld();
+        for (int c2 = 64 * half; c2 < 64 * half + 64; c2 += 32) {
+          float ff[2][16];
+          tmem_ld16(tmem_addr(tmem, 32 * quarter, c2), ff[0]);
+          tmem_ld16(tmem_addr(tmem, 32 * quarter, c2 + 16), ff[1]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float (&f)[16] = ff[hh];
+            const int c0 = c2 + 16 * hh;
             const uint32_t kb = c0 >> 6, kin = c0 & 63;
             const int row = top ? i : 64 + i;
             if (!top) {                                // Q' = (Q~m - P T K~m) Em
@@ -502,19 +633,24 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             for (int e = 0; e < 8; ++e) { lo[e] = f[e] * em[e]; hi[e] = f[8 + e] * em[8 + e]; }
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin)) = pack8(lo);
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = pack8(hi);
+          }
         }
         uint8_t* uo = rec + (top ? TcRec::kU0 : TcRec::kO0);
 #pragma unroll 1
-        for (int t = 4 * half; t < 4 * half + 4; ++t) {
-            float f[16];
-            tmem_ld16(tmem_addr(tmem, 32 * quarter, 128 + t * kTile), f);
+        for (int t2 = 4 * half; t2 < 4 * half + 4; t2 += 2) {
+            float ff[2][16];
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, 128 + t2 * kTile), ff[0]);
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, 128 + (t2 + 1) * kTile), ff[1]);
             tmem_wait_ld();
-            float lo[8], hi[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) { lo[e] = f[e]; hi[e] = f[8 + e]; }
-            uint4* dst = (uint4*)(uo + t * TcRec::kTileBytes + i * (kTile * 2));
-            dst[0] = pack8(lo);
-            dst[1] = pack8(hi);
+            for (int hh = 0; hh < 2; ++hh) {
+                float lo[8], hi[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { lo[e] = ff[hh][e]; hi[e] = ff[hh][8 + e]; }
+                uint4* dst = (uint4*)(uo + (t2 + hh) * TcRec::kTileBytes + i * (kTile * 2));
+                dst[0] = pack8(lo);
+                dst[1] = pack8(hi);
+            }
         }
     } else if (tid == 0) {
         record_status(hdr, KDA_ERR_TIMEOUT);
@@ -528,39 +664,62 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 // ---------------------------------------------------------------------------
 // Kernel (b): the chain over chunks, one CTA per (sequence, head, segment)
 // ---------------------------------------------------------------------------
-// Segments split one sequence's chunks so that long sequences occupy every SM:
-//   phase A (TRANS): each segment p but the last runs the chain from the
-//      augmented state X = [0 | I] (N = 256): it ends at [B_p | M_p], the
-//      affine map  S_end = M_p S_start + B_p  of the segment;
-//   phase B: S_start(p+1) = M_p S_start(p) + B_p, sequential over p, fp32;
-//   phase C (OUT): every segment from its true start state (N = 128), with the
-//      outputs; the last segment writes the final state.
-// A sequence that gets one segment is the plain chain (phase C only).
-// Planning uses a fixed SM count so that the workspace size depends on
-// (N, H, T) only.
+// Segments split one sequence's chunks so that long sequences occupy every SM.
+// Segment 0 is [0, L0) and segment p >= 1 is [L0 + (p-1) L, L0 + p L):
+//   launch 1: segment 0 runs the output pass (OUT, N = 128) from the initial
+//      state, writing its outputs and its end state S_start(1); at the same
+//      time every segment p = 1 .. segs-2 runs the transition pass (TRANS,
+//      N = 256) from the augmented state X = [0 | I]: it ends at [B_p | M_p],
+//      the affine map  S_end = M_p S_start + B_p  of the segment;
+//   launch 2 (phase B): S_start(p+1) = M_p S_start(p) + B_p, sequential over
+//      p >= 1, fp32;
+//   launch 3: segments 1 .. segs-1 run the output pass from their start
+//      states; the last writes the final state.
+// Segment 0 is longer (L0 ~ 1.3 L) because its output pass shares launch 1
+// with the transitions, whose steps take longer.  A sequence that gets one
+// segment is the plain chain (launch 1 only).  Planning uses a fixed SM count
+// so that the workspace size depends on (N, H, T) only.
 constexpr int kPlanSMs = 152;
 constexpr int kChainWarps = 16;                 // consumer warps (4 per TMEM lane quarter)
 constexpr int kChainThreads = 32 * kChainWarps + 32;
 
 struct ScanPlan {
-    int seg_chunks;   // chunks per segment
+    int len0;         // chunks of segment 0
+    int len;          // chunks of every later segment
     int segs_max;     // segments of the longest possible sequence
 };
 static ScanPlan scan_plan(int N, int H, int64_t T) {
     ScanPlan p;
     const int64_t chunks_max = (T + kChunk - 1) / kChunk;
-    int64_t target = (int64_t)N * H > 0 ? kPlanSMs / ((int64_t)N * H) : 1;
-    if (target < 1) target = 1;
-    int64_t seg = (chunks_max + target - 1) / target;
-    if (seg < 128) seg = 128;                      // short segments are not worth the extra passes
-    p.seg_chunks = (int)seg;
-    p.segs_max = (int)((chunks_max + seg - 1) / seg);
-    if (p.segs_max < 1) p.segs_max = 1;
+    const int64_t nh = (int64_t)N * H;
+    const int64_t target = nh > 0 ? kPlanSMs / nh : 1;    // CTAs per (sequence, head) in launches 1 and 3
+    if (target < 2 || chunks_max <= 2 * 128) {
+        p.len0 = (int)(chunks_max > 0 ? chunks_max : 1);
+        p.len = 1;
+        p.segs_max = 1;
+        return p;
+    }
+    int64_t len = (10 * chunks_max + 10 * target + 12) / (10 * target + 13);   // chunks_max / (target + 1.3)
+    if (len < 128) len = 128;                      // short segments are not worth the extra passes
+    int64_t len0 = (13 * len + 9) / 10;
+    if (len0 + target * len < chunks_max) len0 = chunks_max - target * len;
+    if (len0 > chunks_max) len0 = chunks_max;
+    p.len0 = (int)len0;
+    p.len = (int)len;
+    p.segs_max = chunks_max <= len0 ? 1 : 1 + (int)((chunks_max - len0 + len - 1) / len);
     return p;
 }
 // Segment scratch per (sequence, head, segment): [B_p | M_p] fp32 [128][256] and
 // S_start fp32 [128][128].
 constexpr size_t kSegMB = (size_t)kTcD * 256 * 4, kSegS = (size_t)kTcD * kTcD * 4, kSegBytes = kSegMB + kSegS;
+
+// Number of segments of a sequence of nch chunks, and the first chunk of segment p.
+__host__ __device__ __forceinline__ int seg_count(int nch, int len0, int len) {
+    return nch <= len0 ? 1 : 1 + (nch - len0 + len - 1) / len;
+}
+__host__ __device__ __forceinline__ int seg_begin(int p, int len0, int len) {
+    return p == 0 ? 0 : len0 + (p - 1) * len;
+}
 
 size_t tc_extra_bytes(int N, int H, int64_t T) {
     const ScanPlan p = scan_plan(N, H, T);
@@ -588,15 +747,40 @@ __device__ __forceinline__ uint32_t mn_off(uint32_t row, uint32_t col, uint32_t 
     return (col >> 6) * rows * 128u + sw128_off(row, col & 63u);
 }
 
+// Arguments shared by the chain launches.
+struct ChainArgs {
+    const int32_t* cu;
+    DeviceHeader* hdr;
+    const int32_t* chunk_first;
+    int H, len0, len, segs_max;
+    const uint8_t* recs;
+    const float* initial_state;
+    __nv_bfloat16* out;
+    float* final_state;
+    uint8_t* segbuf;
+    const int32_t* snap_slot;
+    float* snaps;
+};
+
+// One CTA's pass over segment p of sequence-head blockIdx.x: the output pass
+// (NX = 128) or the transition pass (NX = 256).
 template <int NX>
-__global__ void __launch_bounds__(kChainThreads, 1)
-kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, const int32_t* __restrict__ chunk_first,
-             int H, int seg_chunks, const uint8_t* __restrict__ recs, const float* __restrict__ initial_state,
-             __nv_bfloat16* __restrict__ out, float* __restrict__ final_state, uint8_t* __restrict__ segbuf,
-             int segs_max) {
+__device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
+    const int32_t* __restrict__ cu = A.cu;
+    DeviceHeader* __restrict__ hdr = A.hdr;
+    const int32_t* __restrict__ chunk_first = A.chunk_first;
+    const int H = A.H, segs_max = A.segs_max;
+    const uint8_t* __restrict__ recs = A.recs;
+    const float* __restrict__ initial_state = A.initial_state;
+    __nv_bfloat16* __restrict__ out = A.out;
+    float* __restrict__ final_state = A.final_state;
+    uint8_t* __restrict__ segbuf = A.segbuf;
+    const int32_t* __restrict__ snap_slot = A.snap_slot;
+    float* __restrict__ snaps = A.snaps;
     using L = SmemC<NX>;
     constexpr bool kOut = L::kOut;
     constexpr int kCols = NX / 4;                      // columns per consumer warp
+    constexpr int kLdB = NX == 128 ? 2 : 1;             // TMEM loads in flight per wait (register budget)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* full = (uint64_t*)(sm + L::kMisc);     // [2]
@@ -607,12 +791,12 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (hdr->status != KDA_OK) return;
-    const int nh = blockIdx.x, n = nh / H, h = nh % H, p = blockIdx.y;
+    const int nh = blockIdx.x, n = nh / H, h = nh % H;
     const int c_seq = chunk_first[n], nch = chunk_first[n + 1] - c_seq;
-    int segs = (nch + seg_chunks - 1) / seg_chunks;
-    if (segs < 1) segs = 1;
-    if (p >= segs || (!kOut && p >= segs - 1)) return;
-    const int cb = p * seg_chunks, ce = min(nch, cb + seg_chunks);    // chunk range within the sequence
+    const int segs = seg_count(nch, A.len0, A.len);
+    if (p >= segs || (!kOut && (p == 0 || p >= segs - 1))) return;
+    const int cb = seg_begin(p, A.len0, A.len);                 // chunk range within the sequence
+    const int ce = min(nch, seg_begin(p + 1, A.len0, A.len));
     const int nsteps = ce - cb;
     const int64_t seq0 = cu[n], seq1 = cu[n + 1];
     uint8_t* seg = segbuf ? segbuf + ((size_t)nh * segs_max + p) * kSegBytes : nullptr;
@@ -703,6 +887,8 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
         for (int it = 0; it < nsteps && ok; ++it) {
             const int s = it & 1;
             const uint8_t* st = sm + s * L::kStageBytes;
+            // snapshot request for the state after this chunk (output pass only)
+            const int snap_m = (kOut && snap_slot) ? snap_slot[c_seq + cb + it] : -1;
             bool good = mbar_wait(&full[s], (it >> 1) & 1, kWaitNs);
             tc_fence_after_sync();
             if (tid == 0 && good) {
@@ -720,11 +906,15 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
             if (q < 2) {
                 // U = U0 - W X  (the M columns have no U0 term)
 #pragma unroll
-                for (int j = 0; j < kCols; j += 16) {
-                    float d[16];
-                    tmem_ld16(tmem_addr(tmem, 32 * q, col0 + j), d);
-                    tmem_wait_ld();
-                    const int c = col0 + j;
+                for (int j2 = 0; j2 < kCols; j2 += 16 * kLdB) {
+                  float dd[kLdB][16];
+#pragma unroll
+                  for (int hh = 0; hh < kLdB; ++hh) tmem_ld16(tmem_addr(tmem, 32 * q, col0 + j2 + 16 * hh), dd[hh]);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int hh = 0; hh < kLdB; ++hh) {
+                    const float (&d)[16] = dd[hh];
+                    const int c = col0 + j2 + 16 * hh;
                     float lo[8], hi[8];
                     if (c < kTcD) {
                         const uint8_t* u0 = st + L::kU0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2);
@@ -739,6 +929,7 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
                     }
                     *(uint4*)(UO + mn_off(tok, c, 64)) = pack8(lo);
                     *(uint4*)(UO + mn_off(tok, c + 8, 64)) = pack8(hi);
+                  }
                 }
                 fence_proxy_async_smem();
             } else if (kOut) {
@@ -747,11 +938,15 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
                 const int64_t t = seq0 + (int64_t)(cb + it) * kChunk + tok;
                 const bool store = good && t < seq1;
 #pragma unroll
-                for (int j = 0; j < kCols; j += 16) {
-                    float d[16];
-                    tmem_ld16(tmem_addr(tmem, 32 * q, col0 + j), d);
-                    tmem_wait_ld();
-                    const int c = col0 + j;
+                for (int j2 = 0; j2 < kCols; j2 += 16 * kLdB) {
+                  float dd[kLdB][16];
+#pragma unroll
+                  for (int hh = 0; hh < kLdB; ++hh) tmem_ld16(tmem_addr(tmem, 32 * q, col0 + j2 + 16 * hh), dd[hh]);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int hh = 0; hh < kLdB; ++hh) {
+                    const float (&d)[16] = dd[hh];
+                    const int c = col0 + j2 + 16 * hh;
                     const uint8_t* o0 = st + L::kO0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2);
                     float a[8], b[8];
                     unpack8(*(const uint4*)o0, a);
@@ -763,6 +958,7 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
                         dst[0] = pack8(a);
                         dst[1] = pack8(b);
                     }
+                  }
                 }
             }
             tc_fence_before_sync();
@@ -780,12 +976,20 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
             tc_fence_after_sync();
             const float gam = ((const float*)(st + L::kGam))[i];
 #pragma unroll
-            for (int j = 0; j < kCols; j += 16) {
-                float d[16];
-                tmem_ld16(tmem_addr(tmem, 32 * q, NX + col0 + j), d);
+            for (int j = 0; j < kCols; j += 16 * kLdB) {
+                float d[kLdB][16];
+#pragma unroll
+                for (int hh = 0; hh < kLdB; ++hh) tmem_ld16(tmem_addr(tmem, 32 * q, NX + col0 + j + 16 * hh), d[hh]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) X[j + e] = fmaf(gam, X[j + e], d[e]);
+                for (int hh = 0; hh < kLdB; ++hh)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) X[j + 16 * hh + e] = fmaf(gam, X[j + 16 * hh + e], d[hh][e]);
+            }
+            if (kOut && snap_m >= 0 && good) {
+                float* dst = snaps + (((size_t)snap_m * H + h) * kTcD + i) * kTcD + col0;
+#pragma unroll
+                for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
             }
             write_X(1.f);
             fence_proxy_async_smem();
@@ -797,8 +1001,13 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
             *(volatile int*)s_abort = 1;
             if (tid == 0) record_status(hdr, KDA_ERR_TIMEOUT);
         } else if (kOut) {
-            if (p == segs - 1 && final_state) {
-                float* dst = final_state + ((size_t)nh * kTcD + i) * kTcD + col0;
+            float* dst = nullptr;
+            if (p == segs - 1) {
+                if (final_state) dst = final_state + ((size_t)nh * kTcD + i) * kTcD + col0;
+            } else if (p == 0) {       // segment 0 hands its end state to segment 1
+                dst = (float*)(segbuf + ((size_t)nh * segs_max + 1) * kSegBytes + kSegMB) + (size_t)i * kTcD + col0;
+            }
+            if (dst) {
 #pragma unroll
                 for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
             }
@@ -813,24 +1022,40 @@ kda_tc_chain(const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr, con
     if (warp == 0) tmem_dealloc(tmem, 2 * NX);
 }
 
-// Phase B: S_start(p+1) = M_p S_start(p) + B_p for one (sequence, head) and a
+// Launch 1: segment 0's output pass (blockIdx.y == 0) beside the transition
+// passes of segments 1 .. segs-2 (blockIdx.y = p).
+__global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_first(const ChainArgs A) {
+    if (A.hdr->status != KDA_OK) return;
+    if (blockIdx.y == 0) chain_segment<128>(A, 0);
+    else chain_segment<256>(A, blockIdx.y);
+}
+
+// Launch 3: the output passes of segments 1 .. segs-1 (p = blockIdx.y + 1).
+__global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_rest(const ChainArgs A) {
+    if (A.hdr->status != KDA_OK) return;
+    chain_segment<128>(A, blockIdx.y + 1);
+}
+
+// Phase B: S_start(p+1) = M_p S_start(p) + B_p for p = 1 .. segs-2, from
+// S_start(1) (segment 0's end state), for one (sequence, head) and a
 // 16-column block of the state (columns of S are independent), fp32.
 __global__ void __launch_bounds__(256)
-kda_tc_scan_states(const int32_t* __restrict__ chunk_first, DeviceHeader* __restrict__ hdr, int H, int seg_chunks,
-                   const float* __restrict__ initial_state, uint8_t* __restrict__ segbuf, int segs_max) {
+kda_tc_scan_states(const int32_t* __restrict__ chunk_first, DeviceHeader* __restrict__ hdr, int H, int len0,
+                   int len, uint8_t* __restrict__ segbuf, int segs_max) {
     if (hdr->status != KDA_OK) return;
     const int nh = blockIdx.x, n = nh / H, cblk = blockIdx.y * 16;
     const int nch = chunk_first[n + 1] - chunk_first[n];
-    const int segs = (nch + seg_chunks - 1) / seg_chunks;
-    if (segs < 2) return;
+    const int segs = seg_count(nch, len0, len);
+    if (segs < 3) return;
     __shared__ float S[kTcD][16];
     const int tid = threadIdx.x, row = tid >> 1, half = (tid & 1) * 8;
+    const float* S1 = (const float*)(segbuf + ((size_t)nh * segs_max + 1) * kSegBytes + kSegMB);
     for (int e = tid; e < kTcD * 16; e += 256) {
         const int r = e >> 4, cc = e & 15;
-        S[r][cc] = initial_state ? initial_state[((size_t)nh * kTcD + r) * kTcD + cblk + cc] : 0.f;
+        S[r][cc] = S1[(size_t)r * kTcD + cblk + cc];
     }
     __syncthreads();
-    for (int p = 0; p + 1 < segs; ++p) {
+    for (int p = 1; p + 1 < segs; ++p) {
         const float* MB = (const float*)(segbuf + ((size_t)nh * segs_max + p) * kSegBytes);
         const float* Mrow = MB + (size_t)row * 256 + kTcD;       // M_p row `row`
         float acc[8];
@@ -884,38 +1109,43 @@ static bool make_v_map(CUtensorMap* m, const void* base, int64_t T, int H) {
 
 cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stream) {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(kda_tc_intra_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto intra = a.la_scalar ? kda_tc_intra_chunk<true> : kda_tc_intra_chunk<false>;
+    if ((e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)SmemA::kBytes)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(kda_tc_chain<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)SmemC<128>::kBytes)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(kda_tc_chain<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(kda_tc_chain_first, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)SmemC<256>::kBytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kda_tc_chain_rest, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)SmemC<128>::kBytes)) != cudaSuccess) return e;
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[0], stream)) != cudaSuccess) return e;
     if (a.chunks_ub > 0 && T > 0) {
         CUtensorMap mv;
         if (!make_v_map(&mv, a.v, T, a.H)) return cudaErrorInvalidValue;
-        kda_tc_intra_chunk<<<dim3(a.chunks_ub, a.H), kAThreads, SmemA::kBytes, stream>>>(
+        intra<<<dim3(a.chunks_ub, a.H), kAThreads, SmemA::kBytes, stream>>>(
             mv, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.la,
-            a.la_scalar, (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, (uint8_t*)a.recs);
+            (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, (uint8_t*)a.recs);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[1], stream)) != cudaSuccess) return e;
     const ScanPlan plan = scan_plan(a.N, a.H, T);
-    uint8_t* segbuf = plan.segs_max > 1 ? (uint8_t*)a.extra : nullptr;
-    const dim3 grid((unsigned)a.N * a.H, plan.segs_max);
-    if (segbuf) {
-        kda_tc_chain<256><<<grid, kChainThreads, SmemC<256>::kBytes, stream>>>(
-            a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.H, plan.seg_chunks, (const uint8_t*)a.recs, a.s0,
-            (__nv_bfloat16*)a.out, a.sf, segbuf, plan.segs_max);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        kda_tc_scan_states<<<dim3((unsigned)a.N * a.H, kTcD / 16), 256, 0, stream>>>(
-            a.chunk_first, (DeviceHeader*)a.hdr, a.H, plan.seg_chunks, a.s0, segbuf, plan.segs_max);
+    ChainArgs ca;
+    ca.cu = a.cu; ca.hdr = (DeviceHeader*)a.hdr; ca.chunk_first = a.chunk_first; ca.H = a.H;
+    ca.len0 = plan.len0; ca.len = plan.len; ca.segs_max = plan.segs_max;
+    ca.recs = (const uint8_t*)a.recs; ca.initial_state = a.s0; ca.out = (__nv_bfloat16*)a.out;
+    ca.final_state = a.sf; ca.segbuf = plan.segs_max > 1 ? (uint8_t*)a.extra : nullptr;
+    ca.snap_slot = a.snap_slot; ca.snaps = a.snaps;
+    const unsigned nh = (unsigned)a.N * a.H;
+    const unsigned ylaunch = plan.segs_max > 1 ? (unsigned)plan.segs_max - 1 : 1;
+    kda_tc_chain_first<<<dim3(nh, ylaunch), kChainThreads, SmemC<256>::kBytes, stream>>>(ca);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (plan.segs_max > 1) {
+        if (plan.segs_max > 2) {
+            kda_tc_scan_states<<<dim3(nh, kTcD / 16), 256, 0, stream>>>(
+                a.chunk_first, (DeviceHeader*)a.hdr, a.H, plan.len0, plan.len, ca.segbuf, plan.segs_max);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        kda_tc_chain_rest<<<dim3(nh, ylaunch), kChainThreads, SmemC<128>::kBytes, stream>>>(ca);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    kda_tc_chain<128><<<grid, kChainThreads, SmemC<128>::kBytes, stream>>>(
-        a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.H, plan.seg_chunks, (const uint8_t*)a.recs, a.s0,
-        (__nv_bfloat16*)a.out, a.sf, segbuf, plan.segs_max);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[2], stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }

@@ -117,6 +117,22 @@ def test_scalar_gate_alignment():
         kda.KDA_ERR_INVALID_ARGUMENT
 
 
+def test_snapshot_host_validation():
+    import torch
+    q, k, v, la, b, cu, s0, out, sf, ws = _ptrs()
+    at, snaps = _FakePtr(ws.addr + (1 << 24)), _FakePtr(ws.addr + 2 * (1 << 24))
+    d = kda.make_desc(2, 4, 128, 128, 256, torch.bfloat16)
+    call = lambda m, a, sn: kda.kda_prefill_snapshots(d, q, k, v, la, b, cu, s0, out, sf, m, a, sn, 0)
+    assert call(-1, at, snaps) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert call(3, None, snaps) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert call(3, at, None) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert call(3, _FakePtr(at.addr + 2), snaps) == kda.KDA_ERR_INVALID_ARGUMENT     # 4-byte pairs
+    assert call(3, at, _FakePtr(snaps.addr + 8)) == kda.KDA_ERR_INVALID_ARGUMENT     # 16-byte states
+    assert call(3, at, _FakePtr(sf.addr + 4096)) == kda.KDA_ERR_INVALID_ARGUMENT     # overlaps final state
+    assert call(3, at, snaps) == kda.KDA_ERR_WORKSPACE          # arguments fine, no workspace given
+    assert call(0, None, None) == kda.KDA_ERR_WORKSPACE
+
+
 def test_decode_host_validation():
     import torch
     q, k, v, la, b, st, out = _ptrs(n=7)
