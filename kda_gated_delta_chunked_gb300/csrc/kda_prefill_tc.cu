@@ -31,13 +31,12 @@
 //   3. With A^[i][j] = beta_j (K~ K^T)[i][j] (j < i), the rows of
 //      Y^ = [T; P T] solve  Y^ (I + A^) = [Diag(beta); P Diag(beta)]  (beta
 //      folded into the columns, so the solution needs no later rescaling).
-//      The solve runs in 16-column blocks from the right.  The inverses E_J
-//      of the four 16 x 16 diagonal blocks are formed first (fp32 forward
-//      substitution, one thread per column), then in parallel the blocks'
-//      right-hand sides times E_J and the coupling blocks A^_KJ E_J; what
-//      remains sequential is one small MMA per block (M=128, N=16, from the
-//      bf16 Y^ and the coupling blocks stored row by row, read MN-major) and a
-//      subtraction.
+//      The solve runs in 16-column blocks from the right: the coupling to the
+//      already solved blocks is one small MMA (M=128, N=16) from the bf16 Y^
+//      and A^ (stored row by row, read MN-major), the 16 x 16 diagonal block a
+//      short fp32 recursion.  (Forming the diagonal-block inverses first, so
+//      that the sequential part is only the MMAs, was measured 1% slower: the
+//      recursion's work moves, it does not shrink.)
 //   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~m | V] with K~m read MN-major
 //      from the MMA-a operand; since K~ = K~m Diag(2^g_m), W, P T K~ and Q~
 //      are rescaled per channel in the epilogue, Q' = Q~ - P T K~.
@@ -112,7 +111,6 @@ struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per 
     static constexpr uint32_t kOpB1 = 49152;    // MMA-a B K^m, K-major, 2 K-blocks x 8 KB; then:
     static constexpr uint32_t kAt = 49152;      //   A^ by 16-column blocks, MN-major 32B-swizzle, 4 x 2 KB
     static constexpr uint32_t kAt32 = 57344;    //   diagonal 16 x 16 blocks of A^ transposed, fp32, 4 KB
-    static constexpr uint32_t kE32 = 61440;     //   E_J = (I + A^_JJ)^-1 of the diagonal blocks, fp32, 4 KB
     static constexpr uint32_t kY = 65536;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB
     static constexpr uint32_t kPart = 65536;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
     static constexpr uint32_t kGS = 49152;      // (slow path, before A^) g, fp32 [64][128], 32 KB
@@ -136,52 +134,18 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                       pack_bf16x2(f[6], f[7]));
 }
 
-// The solve Y^ (I + A^) = RHS, RHS = [Diag(beta); P Diag(beta)], by 16-column
-// blocks J = 3..0.  With D_J = I + A^_JJ (unit lower triangular) and
-// E_J = D_J^-1, block J of the solution is
-//     Y^_J = RHS_J E_J - sum_{K>J} Y^_K (A^_KJ E_J),
-// so once the four E_J, the right-hand sides R'_J = RHS_J E_J and the coupling
-// blocks M_KJ = A^_KJ E_J are formed (all independent of Y^, computed in
-// parallel), the sequential part is one small MMA per block (Y^_K M_KJ into
-// TMEM columns 64..79) and a subtraction: no recursion on the critical path.
-
-// y[c] = sum_{l >= c} r[l] E[l][c] for one 16-wide row r and E = E_J (fp32,
-// row-major [16][16] in shared memory, lower triangular).
-__device__ __forceinline__ void row_times_e(const float (&r)[16], const float* E, float (&y)[16]) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) y[c] = 0.f;
-#pragma unroll
-    for (int l = 0; l < 16; ++l) {
-        const float4* e4 = (const float4*)(E + 16 * l);
-#pragma unroll
-        for (int g = 0; g <= (l >> 2); ++g) {
-            const float4 e = e4[g];
-            if (4 * g + 0 <= l) y[4 * g + 0] = fmaf(r[l], e.x, y[4 * g + 0]);
-            if (4 * g + 1 <= l) y[4 * g + 1] = fmaf(r[l], e.y, y[4 * g + 1]);
-            if (4 * g + 2 <= l) y[4 * g + 2] = fmaf(r[l], e.z, y[4 * g + 2]);
-            if (4 * g + 3 <= l) y[4 * g + 3] = fmaf(r[l], e.w, y[4 * g + 3]);
-        }
-    }
-}
-
-// Stores 16 values as bf16 into columns 16J..16J+15 of row `row` of Y^.
-__device__ __forceinline__ void store_y16(uint8_t* yop, int row, int J, const float (&y)[16]) {
-    float lo[8], hi[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) { lo[e] = y[e]; hi[e] = y[8 + e]; }
-    *(uint4*)(yop + sw128_off(row, 16 * J)) = pack8(lo);
-    *(uint4*)(yop + sw128_off(row, 16 * J + 8)) = pack8(hi);
-}
-
-// Block J < 3 of the sequential part: the coupling MMA, then Y^_J = R'_J - it.
-// Rows 0..63 are finished by warps 0,1 (R' nonzero only in the row's own
-// block), rows 64..127 by the two warps of lane quarters 2,3 that hold R'_J.
+// Column block J (16 columns) of the solve Y^ (I + A^) = RHS for row `tid`
+// (threads 0..127) of Y^: the right-hand side (from the Gram / Q~ K^T
+// accumulator still in TMEM columns 0..63), minus the coupling to the solved
+// blocks on the right (one MMA from the bf16 Y^ and A^ into TMEM columns
+// 64..79), then the in-block recursion on the fp32 diagonal block; stored to
+// Y^ as bf16.  Threads 128..255 only take part in the barrier.
 template <int J>
-__device__ __forceinline__ void solve_block(uint8_t* sm, uint32_t tmem, uint64_t* bar, int* s_flag, uint32_t& mph,
-                                            bool& abort, const float (&y0)[16], const float (&yP)[2][16]) {
-    const int tid = threadIdx.x, warp = tid >> 5, quarter = warp & 3;
+__device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const float* s_beta, uint64_t* bar,
+                                          int* s_flag, uint32_t& mph, bool& abort) {
+    const int tid = threadIdx.x, warp = tid >> 5;
     uint8_t* yop = sm + SmemA::kY;
-    if (tid == 0 && !abort) {
+    if (J < 3 && tid == 0 && !abort) {
 #pragma unroll
         for (int ks = J + 1; ks < 4; ++ks)
             mma_bf16_ss(tmem + 64, sdesc_k_sw128(smem_u32(yop + ks * 32)),
@@ -189,27 +153,50 @@ __device__ __forceinline__ void solve_block(uint8_t* sm, uint32_t tmem, uint64_t
                         idesc_bf16(128, 16, 0, 1), ks > J + 1);
         mma_commit(bar);
     }
-    const bool top = warp < 2;
-    const bool bottom = quarter >= 2 && ((warp < 4) == (J >= 2));
-    if (top || bottom) {
-        if (!abort && !mbar_wait(bar, mph & 1, kWaitNs)) s_flag[1] = 1;
-        tc_fence_after_sync();
-        float d[16], y[16];
-        tmem_ld16(tmem_addr(tmem, 32 * quarter, 64), d);
-        tmem_wait_ld();
-        if (top) {
-            const bool own = (tid >> 4) == J;          // row tid lies in block J
+    if (warp < 4) {
+        const float4* at32v = (const float4*)(sm + SmemA::kAt32);
+        float z[16];
+        if (warp < 2) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) y[c] = (own ? y0[c] : 0.f) - d[c];
-            store_y16(yop, tid, J, y);
+            for (int jj = 0; jj < 16; ++jj) z[jj] = (16 * J + jj == tid) ? s_beta[tid] : 0.f;
         } else {
+            const int i = tid - 64;
+            float f[16];
+            tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * J), f);
+            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 16; ++c) y[c] = yP[J & 1][c] - d[c];
-            store_y16(yop, 64 + (quarter & 1) * 32 + (tid & 31), J, y);
+            for (int jj = 0; jj < 16; ++jj) z[jj] = (16 * J + jj <= i) ? f[jj] * s_beta[16 * J + jj] : 0.f;
         }
+        if (J < 3) {
+            if (!abort && !mbar_wait(bar, mph & 1, kWaitNs)) s_flag[1] = 1;
+            tc_fence_after_sync();
+            float dd[16];
+            tmem_ld16(tmem_addr(tmem, 32 * warp, 64), dd);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) z[jj] -= dd[jj];
+        }
+#pragma unroll
+        for (int jj = 14; jj >= 0; --jj) {
+            float acc = z[jj];
+#pragma unroll
+            for (int g4 = (jj + 1) >> 2; g4 < 4; ++g4) {
+                const float4 a = at32v[(J * 16 + jj) * 4 + g4];
+                if (4 * g4 + 0 > jj) acc = fmaf(-z[4 * g4 + 0], a.x, acc);
+                if (4 * g4 + 1 > jj) acc = fmaf(-z[4 * g4 + 1], a.y, acc);
+                if (4 * g4 + 2 > jj) acc = fmaf(-z[4 * g4 + 2], a.z, acc);
+                if (4 * g4 + 3 > jj) acc = fmaf(-z[4 * g4 + 3], a.w, acc);
+            }
+            z[jj] = acc;
+        }
+        uint32_t p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p[e] = pack_bf16x2(z[2 * e], z[2 * e + 1]);
+        *(uint4*)(yop + sw128_off(tid, 16 * J)) = make_uint4(p[0], p[1], p[2], p[3]);
+        *(uint4*)(yop + sw128_off(tid, 16 * J + 8)) = make_uint4(p[4], p[5], p[6], p[7]);
         fence_proxy_async_smem();
     }
-    ++mph;
+    if (J < 3) ++mph;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -276,8 +263,6 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             const bool ok = r < len;
             const size_t gi = base + (size_t)r * rs;
             const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-            kr[i] = ok ? *(const uint4*)(k + gi) : z4;
-            qr[i] = ok ? *(const uint4*)(q + gi) : z4;
             float la[8];
             if (kScalarGate) {                  // one gate per (token, head), all channels
                 const float l = ok ? __bfloat162float(log_alpha[(size_t)(t0 + r) * H + h]) : 0.f;
@@ -286,6 +271,8 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             } else {
                 unpack8(ok ? *(const uint4*)(log_alpha + gi) : z4, la);
             }
+            kr[i] = ok ? *(const uint4*)(k + gi) : z4;
+            qr[i] = ok ? *(const uint4*)(q + gi) : z4;
 #pragma unroll
             for (int e = 0; e < 8; ++e) { s8[e] = fmaf(la[e], kLog2e, s8[e]); gl[i][e] = s8[e]; }
         }
@@ -465,113 +452,10 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     tc_fence_after_sync();
 
     // ---- Y^ (I + A^) = [Diag(beta); P Diag(beta)], 16-column blocks from the right.
-    {
-        const int quarter = warp & 3;
-        float* e32 = (float*)(sm + SmemA::kE32);
-        float y0[16], yP[2][16];
-        // (i) rows 64..127 of the right-hand side, P Diag(beta) (P = Q~ K^T,
-        // j <= i): lane quarters 2,3; warps 2,3 take blocks 2,3, warps 6,7 blocks 0,1.
-        if (quarter >= 2) {
-            const int jb = warp < 4 ? 2 : 0, i = (quarter & 1) * 32 + lane;
-            tmem_ld16(tmem_addr(tmem, 32 * quarter, 16 * jb), yP[0]);
-            tmem_ld16(tmem_addr(tmem, 32 * quarter, 16 * jb + 16), yP[1]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int j = 16 * (jb + b) + c;
-                    yP[b][c] = j <= i ? yP[b][c] * s_beta[j] : 0.f;
-                }
-        }
-        // (ii) E_J = (I + L)^-1, L = A^_JJ strictly lower: column c of E by
-        // forward substitution, E[l][c] = delta_lc - sum_{m<l} L[l][m] E[m][c],
-        // in right-looking order (once E[m][c] is final it updates every later
-        // row), so the dependent chain is one FMA per row.
-        if (tid < 64) {
-            const int J = tid >> 4, c = tid & 15;
-            const float4* at4 = (const float4*)(sm + SmemA::kAt32) + J * 64;   // column m of L: at4[4m .. 4m+3]
-            float e[16];
-#pragma unroll
-            for (int l = 0; l < 16; ++l) e[l] = l == c ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < 15; ++m) {
-                float lc[16];
-#pragma unroll
-                for (int g = (m + 1) >> 2; g < 4; ++g) {
-                    const float4 v = at4[4 * m + g];
-                    lc[4 * g] = v.x; lc[4 * g + 1] = v.y; lc[4 * g + 2] = v.z; lc[4 * g + 3] = v.w;
-                }
-#pragma unroll
-                for (int l = m + 1; l < 16; ++l) e[l] = fmaf(-lc[l], e[m], e[l]);
-            }
-#pragma unroll
-            for (int l = 0; l < 16; ++l) e32[(16 * J + l) * 16 + c] = e[l];
-        }
-        __syncthreads();
-        // (iii) R'_J = RHS_J E_J.  Rows 0..63: RHS = Diag(beta), so row i is
-        // beta_i times row (i mod 16) of E_{i/16} (zero in the other blocks).
-        if (quarter >= 2) {
-            const int jb = warp < 4 ? 2 : 0;
-            float r[16];
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-#pragma unroll
-                for (int c = 0; c < 16; ++c) r[c] = yP[b][c];
-                row_times_e(r, e32 + (jb + b) * 256, yP[b]);
-            }
-        } else if (warp < 2) {
-            const float bi = s_beta[tid];
-            const float4* e4 = (const float4*)(e32 + (tid >> 4) * 256 + (tid & 15) * 16);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const float4 e = e4[g];
-                y0[4 * g] = bi * e.x; y0[4 * g + 1] = bi * e.y; y0[4 * g + 2] = bi * e.z; y0[4 * g + 3] = bi * e.w;
-            }
-        }
-        // (iv) coupling blocks M_KJ = A^_KJ E_J (K > J), in place of A^_KJ in the
-        // bf16 MN-major blocks the coupling MMAs read: warps 0,1,4, one row each.
-        if (warp < 2 || warp == 4) {
-            const int u = warp < 2 ? tid : tid - 64;          // 0..95
-            const int pair = u >> 4, a = u & 15;
-            const int K = pair < 3 ? pair + 1 : (pair < 5 ? pair - 1 : 3);
-            const int J = pair < 3 ? 0 : (pair < 5 ? 1 : 2);
-            uint8_t* blk = sm + SmemA::kAt + J * 2048;
-            const int row = 16 * K + a;
-            float r[16], m[16];
-            {
-                float lo[8], hi[8];
-                unpack8(*(const uint4*)(blk + sw32_off(row, 0)), lo);
-                unpack8(*(const uint4*)(blk + sw32_off(row, 8)), hi);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) { r[e] = lo[e]; r[8 + e] = hi[e]; }
-            }
-            row_times_e(r, e32 + J * 256, m);
-            float lo[8], hi[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { lo[e] = m[e]; hi[e] = m[8 + e]; }
-            *(uint4*)(blk + sw32_off(row, 0)) = pack8(lo);
-            *(uint4*)(blk + sw32_off(row, 8)) = pack8(hi);
-        }
-        // (v) block 3 has nothing on its right: Y^_3 = R'_3.
-        if (warp < 2) {
-            float y[16];
-            const bool own = (tid >> 4) == 3;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) y[c] = own ? y0[c] : 0.f;
-            store_y16(sm + SmemA::kY, tid, 3, y);
-        } else if (warp == 2 || warp == 3) {
-            store_y16(sm + SmemA::kY, 64 + (quarter & 1) * 32 + lane, 3, yP[1]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        tc_fence_after_sync();
-        abort = s_flag[1] != 0;
-        solve_block<2>(sm, tmem, &bars[1], s_flag, mph, abort, y0, yP);
-        solve_block<1>(sm, tmem, &bars[1], s_flag, mph, abort, y0, yP);
-        solve_block<0>(sm, tmem, &bars[1], s_flag, mph, abort, y0, yP);
-    }
+    inv_block<3>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
+    inv_block<2>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
+    inv_block<1>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
+    inv_block<0>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
 
     // ---- MMA-b: Y^ [K~m | V] -> [[W Em^-1, U0], [P T K~m, O0]].  Its issuing
     // thread waits for the V tile first (the MMA reads it).
@@ -605,15 +489,10 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         uint8_t* a1 = rec + TcRec::kA1;
         const uint8_t* qm = sm + SmemA::kOpA;
 #pragma unroll 1
-        for (int c2 = 64 * half; c2 < 64 * half + 64; c2 += 32) {
-          float ff[2][16];
-          tmem_ld16(tmem_addr(tmem, 32 * quarter, c2), ff[0]);
-          tmem_ld16(tmem_addr(tmem, 32 * quarter, c2 + 16), ff[1]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float (&f)[16] = ff[hh];
-            const int c0 = c2 + 16 * hh;
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
+            float f[16];
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, c0), f);
+            tmem_wait_ld();
             const uint32_t kb = c0 >> 6, kin = c0 & 63;
             const int row = top ? i : 64 + i;
             if (!top) {                                // Q' = (Q~m - P T K~m) Em
@@ -633,24 +512,19 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             for (int e = 0; e < 8; ++e) { lo[e] = f[e] * em[e]; hi[e] = f[8 + e] * em[8 + e]; }
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin)) = pack8(lo);
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = pack8(hi);
-          }
         }
         uint8_t* uo = rec + (top ? TcRec::kU0 : TcRec::kO0);
 #pragma unroll 1
-        for (int t2 = 4 * half; t2 < 4 * half + 4; t2 += 2) {
-            float ff[2][16];
-            tmem_ld16(tmem_addr(tmem, 32 * quarter, 128 + t2 * kTile), ff[0]);
-            tmem_ld16(tmem_addr(tmem, 32 * quarter, 128 + (t2 + 1) * kTile), ff[1]);
+        for (int t = 4 * half; t < 4 * half + 4; ++t) {
+            float f[16];
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, 128 + t * kTile), f);
             tmem_wait_ld();
+            float lo[8], hi[8];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float lo[8], hi[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) { lo[e] = ff[hh][e]; hi[e] = ff[hh][8 + e]; }
-                uint4* dst = (uint4*)(uo + (t2 + hh) * TcRec::kTileBytes + i * (kTile * 2));
-                dst[0] = pack8(lo);
-                dst[1] = pack8(hi);
-            }
+            for (int e = 0; e < 8; ++e) { lo[e] = f[e]; hi[e] = f[8 + e]; }
+            uint4* dst = (uint4*)(uo + t * TcRec::kTileBytes + i * (kTile * 2));
+            dst[0] = pack8(lo);
+            dst[1] = pack8(hi);
         }
     } else if (tid == 0) {
         record_status(hdr, KDA_ERR_TIMEOUT);
