@@ -85,6 +85,8 @@ class Oracle:
         lib.kda_oracle_prefill.restype = ctypes.c_int
         lib.kda_oracle_decode_step.argtypes = [i32, i32, i32, i32, dp, dp, dp, dp, dp, dp, dp, i32]
         lib.kda_oracle_decode_step.restype = ctypes.c_int
+        lib.kda_oracle_backward.argtypes = [i32, i32, i32, i32, ip] + [dp] * 14 + [i32]
+        lib.kda_oracle_backward.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -118,6 +120,43 @@ class Oracle:
             raise RuntimeError(f"kda_oracle_prefill failed: {rc}")
         return out, sf
 
+    def backward(self, q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, dout=None,
+                 dfinal=None, threads: Optional[int] = None):
+        """fp64 gradients of a scalar loss through the prefill, given its
+        gradients ``dout`` [T,H,d_v] and ``dfinal`` [N,H,d_k,d_v] (None: zero).
+
+        Returns a dict of float64 arrays: dq, dk, dv, dlog_alpha (the shape of
+        ``log_alpha``: a scalar gate [T,H] gets the sum over channels), dbeta,
+        dinitial_state."""
+        q, k, v, la, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
+        T, H, dk = q.shape
+        dv = v.shape[2]
+        scalar_gate = la.ndim == 2
+        la = _per_channel(la, dk)
+        if cu_seqlens is None:
+            cu = np.array([0, T], dtype=np.int32)
+        else:
+            if hasattr(cu_seqlens, "cpu"):
+                cu_seqlens = cu_seqlens.cpu().numpy()
+            cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+        N = len(cu) - 1
+        s0 = None if initial_state is None else _f64(initial_state).reshape(N, H, dk, dv)
+        do = _f64(dout).reshape(T, H, dv)
+        dfin = None if dfinal is None else _f64(dfinal).reshape(N, H, dk, dv)
+        g = {"dq": np.zeros((T, H, dk)), "dk": np.zeros((T, H, dk)), "dv": np.zeros((T, H, dv)),
+             "dlog_alpha": np.zeros((T, H, dk)), "dbeta": np.zeros((T, H)),
+             "dinitial_state": np.zeros((N, H, dk, dv))}
+        rc = self.lib.kda_oracle_backward(N, H, dk, dv, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                          _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(s0), _ptr(do),
+                                          _ptr(dfin), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                                          _ptr(g["dlog_alpha"]), _ptr(g["dbeta"]), _ptr(g["dinitial_state"]),
+                                          threads or default_threads())
+        if rc != 0:
+            raise RuntimeError(f"kda_oracle_backward failed: {rc}")
+        if scalar_gate:
+            g["dlog_alpha"] = g["dlog_alpha"].sum(axis=2)
+        return g
+
     def decode_step(self, q, k, v, log_alpha, beta, state, threads: Optional[int] = None):
         """fp64 decode step.  Inputs [N,H,*]; returns (out [N,H,d_v], new_state)."""
         q, k, v, la, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
@@ -148,3 +187,8 @@ def prefill(*args, **kwargs):
 def decode_step(*args, **kwargs):
     """fp64 decode step with the default oracle build (see ``Oracle.decode_step``)."""
     return default().decode_step(*args, **kwargs)
+
+
+def backward(*args, **kwargs):
+    """fp64 prefill gradients with the default oracle build (see ``Oracle.backward``)."""
+    return default().backward(*args, **kwargs)

@@ -193,3 +193,210 @@ int kda_oracle_decode_step(int32_t num_seqs, int32_t H, int32_t dk, int32_t dv,
     free(cu);
     return rc;
 }
+
+/*
+ * Reverse mode (gradients) of the prefill.  Given the gradient of a scalar
+ * loss with respect to every output, dout [T, H, d_v], and with respect to
+ * the final state, dfinal [N, H, d_k, d_v] (NULL: zero), it returns the
+ * gradients with respect to q, k, v, log_alpha ([T, H, d_k] / [T, H, d_v]),
+ * beta [T, H] and the initial state ds0 [N, H, d_k, d_v] (NULL: not wanted).
+ *
+ * Per sequence and head the forward recurrence above is re-run to recover
+ * the states, then the chain rule is applied to each token's step in reverse
+ * order.  With S' = Diag(alpha_t) S_{t-1}, e = v_t - S'^T k_t,
+ * S_t = S' + beta_t k_t e^T and o_t = S_t^T q_t, and dS the gradient with
+ * respect to S_t (everything after t folded in):
+ *
+ *   read:   dq_t = S_t do_t;            dS += q_t do_t^T
+ *   write:  u = dS^T k_t;  de = beta_t u;  dbeta_t = e . u;  dv_t = de
+ *           dk_t = beta_t dS e - S' de
+ *           dS' = dS - k_t de^T
+ *   decay:  dlog_alpha_t[i] = alpha_t[i] sum_j dS'[i][j] S_{t-1}[i][j]
+ *           dS_{t-1} = Diag(alpha_t) dS'
+ *
+ * and ds0 = dS after the first token.  States are kept at every
+ * kCheckpoint-th token and the ones in between recomputed segment by segment
+ * (the same arithmetic in the same order, so the same values); this bounds
+ * memory at (L / kCheckpoint + kCheckpoint) states per (sequence, head).
+ * Threads split the (sequence, head) pairs.  Returns 0, -1 on bad arguments,
+ * -2 if memory or a thread could not be had.
+ */
+enum { kCheckpoint = 32 };
+
+typedef struct {
+    int32_t num_seqs, H, dk, dv;
+    const int32_t *cu;
+    const double *q, *k, *v, *la, *beta, *s0, *dout, *dfinal;
+    double *dq, *dk_, *dv_, *dla, *dbeta, *ds0;
+    atomic_llong next;
+    atomic_int failed;
+} bjob_t;
+
+/* One forward step of the recurrence on the full state (all columns). */
+static void fwd_step(const bjob_t *B, int64_t t, int32_t h, const double *Sprev, double *Snext,
+                     double *alpha, double *err)
+{
+    const int32_t H = B->H, dk = B->dk, dv = B->dv;
+    const double *kt = B->k + ((size_t)t * H + h) * dk;
+    const double *lat = B->la + ((size_t)t * H + h) * dk;
+    const double *vt = B->v + ((size_t)t * H + h) * dv;
+    const double bt = B->beta[(size_t)t * H + h];
+    for (int32_t i = 0; i < dk; ++i) alpha[i] = exp(lat[i]);
+    for (int32_t i = 0; i < dk; ++i)
+        for (int32_t j = 0; j < dv; ++j)
+            Snext[(size_t)i * dv + j] = alpha[i] * Sprev[(size_t)i * dv + j];
+    for (int32_t j = 0; j < dv; ++j) {
+        double pred = 0.0;
+        for (int32_t i = 0; i < dk; ++i) pred += kt[i] * Snext[(size_t)i * dv + j];
+        err[j] = vt[j] - pred;
+    }
+    for (int32_t i = 0; i < dk; ++i) {
+        const double bk = bt * kt[i];
+        for (int32_t j = 0; j < dv; ++j) Snext[(size_t)i * dv + j] += bk * err[j];
+    }
+}
+
+static int bwd_item(const bjob_t *B, int32_t n, int32_t h)
+{
+    const int32_t H = B->H, dk = B->dk, dv = B->dv;
+    const int64_t t0 = B->cu[n], t1 = B->cu[n + 1], L = t1 - t0;
+    const size_t SZ = (size_t)dk * dv;
+    const size_t sbase = ((size_t)n * H + h) * SZ;
+    const int64_t ncp = L / kCheckpoint + 1;                  /* states at t0 + m * kCheckpoint */
+    double *cp = (double *)malloc(sizeof(double) * SZ * (size_t)ncp);
+    double *seg = (double *)malloc(sizeof(double) * SZ * (kCheckpoint + 1));
+    double *dS = (double *)malloc(sizeof(double) * SZ);
+    double *dSp = (double *)malloc(sizeof(double) * SZ);
+    double *Sp = (double *)malloc(sizeof(double) * SZ);
+    double *alpha = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *err = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *de = (double *)malloc(sizeof(double) * (size_t)dv);
+    int rc = 0;
+    if (!cp || !seg || !dS || !dSp || !Sp || !alpha || !err || !de) { rc = -2; goto done; }
+
+    /* forward: checkpoints */
+    for (size_t e = 0; e < SZ; ++e) cp[e] = B->s0 ? B->s0[sbase + e] : 0.0;
+    {
+        double *cur = seg, *nxt = seg + SZ;
+        memcpy(cur, cp, sizeof(double) * SZ);
+        for (int64_t r = 0; r < L; ++r) {
+            fwd_step(B, t0 + r, h, cur, nxt, alpha, err);
+            double *tmp = cur; cur = nxt; nxt = tmp;
+            if ((r + 1) % kCheckpoint == 0) memcpy(cp + SZ * (size_t)((r + 1) / kCheckpoint), cur, sizeof(double) * SZ);
+        }
+    }
+    /* reverse */
+    for (size_t e = 0; e < SZ; ++e) dS[e] = B->dfinal ? B->dfinal[sbase + e] : 0.0;
+    for (int64_t m = (L - 1) / kCheckpoint; L > 0 && m >= 0; --m) {
+        const int64_t r0 = m * kCheckpoint, r1 = (r0 + kCheckpoint < L) ? r0 + kCheckpoint : L;
+        memcpy(seg, cp + SZ * (size_t)m, sizeof(double) * SZ);          /* seg[s] = state after r0 + s tokens */
+        for (int64_t r = r0; r < r1; ++r)
+            fwd_step(B, t0 + r, h, seg + SZ * (size_t)(r - r0), seg + SZ * (size_t)(r - r0 + 1), alpha, err);
+        for (int64_t r = r1 - 1; r >= r0; --r) {
+            const int64_t t = t0 + r;
+            const double *Sprev = seg + SZ * (size_t)(r - r0);
+            const double *St = seg + SZ * (size_t)(r - r0 + 1);
+            const double *qt = B->q + ((size_t)t * H + h) * dk;
+            const double *kt = B->k + ((size_t)t * H + h) * dk;
+            const double *lat = B->la + ((size_t)t * H + h) * dk;
+            const double *vt = B->v + ((size_t)t * H + h) * dv;
+            const double *dot = B->dout + ((size_t)t * H + h) * dv;
+            const double bt = B->beta[(size_t)t * H + h];
+            /* recompute S' and e for this token */
+            for (int32_t i = 0; i < dk; ++i) alpha[i] = exp(lat[i]);
+            for (int32_t i = 0; i < dk; ++i)
+                for (int32_t j = 0; j < dv; ++j) Sp[(size_t)i * dv + j] = alpha[i] * Sprev[(size_t)i * dv + j];
+            for (int32_t j = 0; j < dv; ++j) {
+                double pred = 0.0;
+                for (int32_t i = 0; i < dk; ++i) pred += kt[i] * Sp[(size_t)i * dv + j];
+                err[j] = vt[j] - pred;
+            }
+            /* read: o_t = S_t^T q_t */
+            for (int32_t i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (int32_t j = 0; j < dv; ++j) acc += St[(size_t)i * dv + j] * dot[j];
+                B->dq[((size_t)t * H + h) * dk + i] = acc;
+                for (int32_t j = 0; j < dv; ++j) dS[(size_t)i * dv + j] += qt[i] * dot[j];
+            }
+            /* write: S_t = S' + beta k e^T, e = v - S'^T k */
+            double db = 0.0;
+            for (int32_t j = 0; j < dv; ++j) {
+                double a = 0.0;
+                for (int32_t i = 0; i < dk; ++i) a += kt[i] * dS[(size_t)i * dv + j];
+                de[j] = bt * a;
+                db += err[j] * a;
+                B->dv_[((size_t)t * H + h) * dv + j] = de[j];
+            }
+            B->dbeta[(size_t)t * H + h] = db;
+            for (int32_t i = 0; i < dk; ++i) {
+                double a = 0.0, b = 0.0;
+                for (int32_t j = 0; j < dv; ++j) {
+                    a += dS[(size_t)i * dv + j] * err[j];
+                    b += Sp[(size_t)i * dv + j] * de[j];
+                }
+                B->dk_[((size_t)t * H + h) * dk + i] = bt * a - b;
+            }
+            for (int32_t i = 0; i < dk; ++i)
+                for (int32_t j = 0; j < dv; ++j) dSp[(size_t)i * dv + j] = dS[(size_t)i * dv + j] - kt[i] * de[j];
+            /* decay: S' = Diag(alpha) S_{t-1} */
+            for (int32_t i = 0; i < dk; ++i) {
+                double a = 0.0;
+                for (int32_t j = 0; j < dv; ++j) a += dSp[(size_t)i * dv + j] * Sprev[(size_t)i * dv + j];
+                B->dla[((size_t)t * H + h) * dk + i] = alpha[i] * a;
+                for (int32_t j = 0; j < dv; ++j) dS[(size_t)i * dv + j] = alpha[i] * dSp[(size_t)i * dv + j];
+            }
+        }
+    }
+    if (B->ds0) memcpy(B->ds0 + sbase, dS, sizeof(double) * SZ);
+done:
+    free(cp); free(seg); free(dS); free(dSp); free(Sp); free(alpha); free(err); free(de);
+    return rc;
+}
+
+static void *bworker(void *arg)
+{
+    bjob_t *B = (bjob_t *)arg;
+    const long long items = (long long)B->num_seqs * B->H;
+    for (;;) {
+        long long it = atomic_fetch_add(&B->next, 1);
+        if (it >= items) break;
+        if (bwd_item(B, (int32_t)(it / B->H), (int32_t)(it % B->H)) != 0) atomic_store(&B->failed, 1);
+    }
+    return NULL;
+}
+
+int kda_oracle_backward(int32_t num_seqs, int32_t H, int32_t dk, int32_t dv,
+                        const int32_t *cu_seqlens,
+                        const double *q, const double *k, const double *v,
+                        const double *log_alpha, const double *beta, const double *initial_state,
+                        const double *dout, const double *dfinal,
+                        double *dq, double *dk_out, double *dv_out, double *dlog_alpha, double *dbeta,
+                        double *dinitial, int32_t num_threads)
+{
+    if (num_seqs < 0 || H <= 0 || dk <= 0 || dv <= 0 || !cu_seqlens) return -1;
+    for (int32_t n = 0; n < num_seqs; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
+    if (num_seqs == 0) return 0;
+    bjob_t B;
+    memset(&B, 0, sizeof(B));
+    B.num_seqs = num_seqs; B.H = H; B.dk = dk; B.dv = dv; B.cu = cu_seqlens;
+    B.q = q; B.k = k; B.v = v; B.la = log_alpha; B.beta = beta; B.s0 = initial_state;
+    B.dout = dout; B.dfinal = dfinal;
+    B.dq = dq; B.dk_ = dk_out; B.dv_ = dv_out; B.dla = dlog_alpha; B.dbeta = dbeta; B.ds0 = dinitial;
+    atomic_init(&B.next, 0);
+    atomic_init(&B.failed, 0);
+    const long long items = (long long)num_seqs * H;
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > items) num_threads = (int32_t)items;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)num_threads);
+    if (!th) return -2;
+    int started = 0;
+    for (int32_t i = 0; i < num_threads; ++i) {
+        if (pthread_create(&th[i], NULL, bworker, &B) != 0) break;
+        ++started;
+    }
+    if (started == 0) bworker(&B);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    return atomic_load(&B.failed) ? -2 : 0;
+}

@@ -311,6 +311,82 @@ def pin_zero_state_default(O):
     _close(s3, np.zeros((1, 2, 4, 3)), 0.0, "empty sequence, zero state")
 
 
+def _fd_check(O, case, cu, coords=None, h=1e-6, tol=1e-7, seed=0):
+    """Central finite differences of L = <wo, out> + <ws, final_state> against
+    the oracle's reverse mode, on every input (or `coords` sampled ones)."""
+    q, k, v, la, b, s0 = case
+    rng = np.random.default_rng(seed)
+    N = len(cu) - 1
+    T, H = q.shape[:2]
+    wo = rng.standard_normal((T, H, v.shape[2]))
+    ws = rng.standard_normal((N, H, k.shape[2], v.shape[2]))
+    g = O.backward(q, k, v, la, b, cu, s0, wo, ws)
+    names = ["q", "k", "v", "log_alpha", "beta", "s0"]
+    keys = ["dq", "dk", "dv", "dlog_alpha", "dbeta", "dinitial_state"]
+    arrs = [q, k, v, la, b, s0]
+
+    def loss(vals):
+        o, sf = O.prefill(*vals[:5], cu, vals[5])
+        return float((o * wo).sum() + (sf * ws).sum())
+
+    for ai, (name, key) in enumerate(zip(names, keys)):
+        idxs = list(np.ndindex(arrs[ai].shape))
+        if coords is not None and len(idxs) > coords:
+            idxs = [idxs[i] for i in rng.choice(len(idxs), coords, replace=False)]
+        for idx in idxs:
+            vals = [a.copy() for a in arrs]
+            vals[ai][idx] += h
+            lp = loss(vals)
+            vals[ai][idx] -= 2 * h
+            lm = loss(vals)
+            fd = (lp - lm) / (2 * h)
+            got = g[key][idx]
+            assert abs(fd - got) <= tol * max(1.0, abs(fd)), \
+                f"d/d{name}{idx}: reverse mode {got:.10g}, finite difference {fd:.10g}"
+
+
+def pin_backward_finite_differences(O):
+    """The reverse mode equals central finite differences of the forward
+    oracle (the definition of the gradient) for every input, on two packed
+    sequences, with d_k != d_v."""
+    rng = np.random.default_rng(RNG_SEED + 20)
+    q, k, v, la, b = _rand_case(rng, 9, 2, 4, 3)
+    s0 = rng.standard_normal((2, 2, 4, 3)) * 0.3
+    _fd_check(O, (q, k, v, la, b, s0), np.array([0, 5, 9], dtype=np.int32))
+
+
+def pin_backward_across_checkpoints(O):
+    """A sequence longer than the oracle's recompute segments (70 tokens):
+    sampled finite differences, including inputs near the start."""
+    rng = np.random.default_rng(RNG_SEED + 21)
+    q, k, v, la, b = _rand_case(rng, 70, 1, 3, 2)
+    s0 = rng.standard_normal((1, 1, 3, 2)) * 0.3
+    _fd_check(O, (q, k, v, la, b, s0), np.array([0, 70], dtype=np.int32), coords=25, seed=1)
+
+
+def pin_backward_scalar_gate(O):
+    """With a scalar gate [T, H] the gate's gradient is that of the shared
+    value: finite differences on the scalar gate itself."""
+    rng = np.random.default_rng(RNG_SEED + 22)
+    q, k, v, la, b = _rand_case(rng, 8, 2, 3, 4)
+    s0 = rng.standard_normal((1, 2, 3, 4)) * 0.3
+    _fd_check(O, (q, k, v, la[:, :, 0].copy(), b, s0), np.array([0, 8], dtype=np.int32), seed=2)
+
+
+def pin_backward_no_write(O):
+    """beta = 0 writes nothing, so neither k nor v can influence anything:
+    their gradients are exactly zero (deep dive, section 03: beta scales
+    the whole correction)."""
+    rng = np.random.default_rng(RNG_SEED + 23)
+    q, k, v, la, b = _rand_case(rng, 12, 2, 4, 3)
+    b[:] = 0.0
+    s0 = rng.standard_normal((1, 2, 4, 3))
+    g = O.backward(q, k, v, la, b, None, s0, rng.standard_normal((12, 2, 3)), rng.standard_normal((1, 2, 4, 3)))
+    assert np.all(g["dk"] == 0.0) and np.all(g["dv"] == 0.0), "beta = 0 but k or v has a gradient"
+
+
 ALL_PINS = [pin_deltanet, pin_gated_deltanet, pin_scalar_gate, pin_no_write, pin_exact_overwrite,
             pin_closed_forms, pin_chunked_form, pin_continuation, pin_varlen_isolation,
-            pin_mode_duality, pin_linearity, pin_exact_rational, pin_zero_state_default]
+            pin_mode_duality, pin_linearity, pin_exact_rational, pin_zero_state_default,
+            pin_backward_finite_differences, pin_backward_across_checkpoints, pin_backward_scalar_gate,
+            pin_backward_no_write]

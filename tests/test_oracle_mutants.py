@@ -27,13 +27,29 @@ MUTANTS = [
     ("read_with_key", "o += qt[i] * S[(size_t)i * dv + j];", "o += kt[i] * S[(size_t)i * dv + j];"),
     ("gate_from_previous_token", "const double *lat = J->la + ((size_t)t * H + h) * dk;",
      "const double *lat = J->la + ((size_t)(t > t0 ? t - 1 : t) * H + h) * dk;"),
+    # reverse mode
+    ("bwd_dk_misses_erase_path", "B->dk_[((size_t)t * H + h) * dk + i] = bt * a - b;",
+     "B->dk_[((size_t)t * H + h) * dk + i] = bt * a;"),
+    ("bwd_dSp_sign", "dSp[(size_t)i * dv + j] = dS[(size_t)i * dv + j] - kt[i] * de[j];",
+     "dSp[(size_t)i * dv + j] = dS[(size_t)i * dv + j] + kt[i] * de[j];"),
+    ("bwd_state_grad_not_decayed", "dS[(size_t)i * dv + j] = alpha[i] * dSp[(size_t)i * dv + j];",
+     "dS[(size_t)i * dv + j] = dSp[(size_t)i * dv + j];"),
+    ("bwd_dq_from_previous_state", "acc += St[(size_t)i * dv + j] * dot[j];",
+     "acc += Sprev[(size_t)i * dv + j] * dot[j];"),
+    ("bwd_dlog_alpha_without_alpha", "B->dla[((size_t)t * H + h) * dk + i] = alpha[i] * a;",
+     "B->dla[((size_t)t * H + h) * dk + i] = a;"),
+    ("bwd_dbeta_uses_value", "db += err[j] * a;", "db += vt[j] * a;"),
+    ("bwd_checkpoint_off_by_one", "memcpy(cp + SZ * (size_t)((r + 1) / kCheckpoint), cur, sizeof(double) * SZ);",
+     "memcpy(cp + SZ * (size_t)((r + 1) / kCheckpoint), nxt, sizeof(double) * SZ);"),
 ]
 
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(tmp_path, name, old, new):
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    # the forward formulas appear in the prefill and again in the reverse mode's
+    # recomputation; a slip is planted everywhere its text appears
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
     mpath = tmp_path / f"{name}.c"
     mpath.write_text(src.replace(old, new))
     lib = oracle.build(force=True, src=str(mpath), out=str(tmp_path / f"lib{name}.so"))
