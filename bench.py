@@ -324,6 +324,10 @@ def run_ours(args, dist: Dist):
     if not args.no_scalar_gate:
         res["scalar_gate"] = bench_scalar_gate(kda, args, stream, x, s0, out, sf, ws, w)
 
+    # --- reverse mode of the prefill (training), on the 4,096-token workload
+    if not args.no_backward:
+        res["backward"] = bench_backward(kda, args, dev, stream)
+
     # --- decode workload (state GB/s)
     if not args.no_decode:
         res["decode"] = bench_decode(kda, args, dev, stream, peaks, peak_src)
@@ -368,6 +372,46 @@ def bench_scalar_gate(kda, args, stream, x, s0, out, sf, ws, w):
     return {"workload": f"{w.name}, log_alpha one per (token, head)", "value": round(T / (ms * 1e-3), 1),
             "unit": "tokens/s", "ms_per_step": round(ms, 4), "steps": steps,
             "gpu_launches": prefill_launches(1, H, T) * steps}
+
+
+def bench_backward(kda, args, dev, stream):
+    """Prefill reverse mode (CUDA cores, fp32) on workload 1: tokens/s."""
+    w = workload(1)
+    T, H, D = w.total_tokens, w.num_heads, w.d_k
+    x = prefill_inputs(w, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(7)
+    do = torch.randn((T, H, D), generator=gen, device=dev, dtype=torch.float32).to(w.torch_dtype)
+    dfin = torch.randn((1, H, D, D), generator=gen, device=dev, dtype=torch.float32)
+    desc = kda.make_desc(1, H, D, D, T, w.torch_dtype)
+    ws = torch.empty(kda.kda_backward_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    desc = kda.make_desc(1, H, D, D, T, w.torch_dtype, ws)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = [torch.empty((T, H, D), **f32) for _ in range(4)] + [torch.empty((T, H), **f32),
+                                                             torch.empty((1, H, D, D), **f32)]
+
+    def run():
+        rc = kda.kda_prefill_backward(desc, x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None,
+                                      x["initial_state"], do, dfin, *g, stream)
+        if rc:
+            raise kda.KdaError("kda_prefill_backward", rc)
+
+    for _ in range(2):
+        run()
+    steps = 3
+    t0, t1 = make_events(2)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        run()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
+        raise RuntimeError("device status not OK (backward)")
+    ms = t0.elapsed_time(t1) / steps
+    return {"workload": w.name, "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms, 3), "steps": steps, "gpu_launches": 3 * steps,
+            "note": "fp32 CUDA cores, one CTA per (sequence, head, 32 state columns); gradients of q, k, v, "
+                    "log_alpha, beta and the initial state"}
 
 
 def bench_decode(kda, args, dev, stream, peaks, peak_src):
@@ -586,6 +630,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scalar-gate", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -175,6 +175,38 @@ KDA_API int kda_prefill_snapshots(const kda_desc *desc,
                                   kda_stream_t stream);
 
 /*
+ * Reverse mode of kda_prefill: the gradients of a scalar loss with respect to
+ * every input, given its gradients with respect to the outputs and the final
+ * state.  The deep dive (section 06) names prefill and training as the uses
+ * of the chunked form; this entry point supplies the training half by the
+ * chain rule through each token's step of the section 03 recurrence.
+ *
+ *   q, k, v, log_alpha, beta, cu_seqlens, initial_state: as for kda_prefill
+ *                    (the same call's inputs).
+ *   d_out            [T_tot, H, d_v], dtype `desc->dtype`: dLoss/dout.
+ *   d_final_state    fp32 [N, H, d_k, d_v] or NULL (zero): dLoss/dfinal_state.
+ *   dq, dk           fp32 [T_tot, H, d_k], written.
+ *   dv               fp32 [T_tot, H, d_v], written.
+ *   dlog_alpha       fp32 [T_tot, H, d_k] ([T_tot, H] with the scalar gate).
+ *   dbeta            fp32 [T_tot, H].
+ *   d_initial_state  fp32 [N, H, d_k, d_v] or NULL (not written).
+ * Gradients are 4-byte aligned, the states 16-byte aligned; no output may
+ * overlap an input or another output.  desc->workspace must hold
+ * kda_backward_workspace_bytes(desc) bytes: about 4 * H * d_k * d_v bytes
+ * per 8 tokens of kept states plus 4 * (3 d_k + 1) * H * d_v / 32 bytes per
+ * token of partial sums.  Runs on CUDA cores in fp32; results do not depend
+ * on scheduling (no atomics).  Errors as for kda_prefill.
+ */
+KDA_API size_t kda_backward_workspace_bytes(const kda_desc *desc);
+KDA_API int kda_prefill_backward(const kda_desc *desc,
+                                 const void *q, const void *k, const void *v,
+                                 const void *log_alpha, const void *beta,
+                                 const int32_t *cu_seqlens, const float *initial_state,
+                                 const void *d_out, const float *d_final_state,
+                                 float *dq, float *dk, float *dv, float *dlog_alpha, float *dbeta,
+                                 float *d_initial_state, kda_stream_t stream);
+
+/*
  * One recurrent decode step for N independent sequences (deep dive section
  * 06, "fused recurrent KDA": decay, correct and write the state in place,
  * reading a fixed amount of memory per head).  Inputs are [N, H, *] (one

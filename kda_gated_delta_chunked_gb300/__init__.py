@@ -15,4 +15,5 @@ from ._binding import (  # noqa: F401
     kda_prefill_workspace_bytes, kda_prefill, kda_decode_step, kda_get_device_status,
     kda_status_string, kda_version, make_desc, prefill, decode_step, kda_prefill_noalloc,
     KDA_PREFILL_NOALLOC_SCRATCH_BYTES, kda_selftest_wait_timeout, kda_prefill_snapshots,
+    kda_backward_workspace_bytes, kda_prefill_backward, prefill_backward,
 )

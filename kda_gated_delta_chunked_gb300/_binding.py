@@ -18,7 +18,8 @@ KDA_FLAG_SCALAR_GATE = 2
 
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_get_device_status",
            "kda_status_string", "kda_last_cuda_error", "kda_version", "kda_prefill_noalloc",
-           "kda_selftest_wait_timeout", "kda_prefill_snapshots")
+           "kda_selftest_wait_timeout", "kda_prefill_snapshots", "kda_backward_workspace_bytes",
+           "kda_prefill_backward")
 KDA_PREFILL_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -52,6 +53,10 @@ def _load():
     L.kda_prefill.restype = ctypes.c_int
     L.kda_prefill_snapshots.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp]
     L.kda_prefill_snapshots.restype = ctypes.c_int
+    L.kda_backward_workspace_bytes.argtypes = [D]
+    L.kda_backward_workspace_bytes.restype = ctypes.c_size_t
+    L.kda_prefill_backward.argtypes = [D] + [vp] * 16
+    L.kda_prefill_backward.restype = ctypes.c_int
     L.kda_prefill_noalloc.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kda_prefill_noalloc.restype = ctypes.c_int
     L.kda_selftest_wait_timeout.argtypes = [D, ctypes.c_int64, vp]
@@ -138,6 +143,50 @@ def kda_prefill_snapshots(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, i
     return lib.kda_prefill_snapshots(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
                                      _p(cu_seqlens), _p(initial_state), _p(out), _p(final_state),
                                      int(num_snapshots), _p(snapshot_at), _p(snapshots), _stream(stream))
+
+
+def kda_backward_workspace_bytes(desc: KdaDesc) -> int:
+    return lib.kda_backward_workspace_bytes(ctypes.byref(desc))
+
+
+def kda_prefill_backward(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, d_out, d_final_state,
+                         dq, dk, dv, dlog_alpha, dbeta, d_initial_state, stream=None) -> int:
+    """Raw C call of the prefill's reverse mode (see include/kda.h)."""
+    return lib.kda_prefill_backward(ctypes.byref(desc), _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
+                                    _p(cu_seqlens), _p(initial_state), _p(d_out), _p(d_final_state), _p(dq),
+                                    _p(dk), _p(dv), _p(dlog_alpha), _p(dbeta), _p(d_initial_state),
+                                    _stream(stream))
+
+
+def prefill_backward(q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, *, d_out,
+                     d_final_state=None, want_initial_grad: bool = True, workspace=None, stream=None):
+    """Gradients of a loss through kda_prefill (fp32 tensors), given d_out and
+    optionally d_final_state.  A 2-D ``log_alpha`` selects the scalar gate.
+    Returns a dict: dq, dk, dv, dlog_alpha, dbeta, d_initial_state (or None)."""
+    T, H, dk_ = q.shape
+    dv_ = v.shape[2]
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta), ("d_out", d_out)):
+        _check(t, name)
+    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = {"dq": torch.empty((T, H, dk_), **f32), "dk": torch.empty((T, H, dk_), **f32),
+         "dv": torch.empty((T, H, dv_), **f32), "dlog_alpha": torch.empty(tuple(log_alpha.shape), **f32),
+         "dbeta": torch.empty((T, H), **f32),
+         "d_initial_state": torch.empty((N, H, dk_, dv_), **f32) if want_initial_grad else None}
+    desc = make_desc(N, H, dk_, dv_, T, q.dtype, flags=flags)
+    if workspace is None:
+        nbytes = kda_backward_workspace_bytes(desc)
+        if nbytes == 0:
+            raise KdaError("kda_backward_workspace_bytes", KDA_ERR_UNSUPPORTED)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    desc.workspace = workspace.data_ptr()
+    desc.workspace_bytes = workspace.numel()
+    rc = kda_prefill_backward(desc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, d_out, d_final_state,
+                              g["dq"], g["dk"], g["dv"], g["dlog_alpha"], g["dbeta"], g["d_initial_state"], stream)
+    if rc != KDA_OK:
+        raise KdaError("kda_prefill_backward", rc)
+    return g
 
 
 def kda_prefill_noalloc(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state,

@@ -284,6 +284,87 @@ int kda_prefill_snapshots(const kda_desc* d, const void* q, const void* k, const
                              num_snapshots, snapshot_at, snapshots, stream);
 }
 
+// Backward workspace: header, chunk table, kept states, per-tile partial sums.
+struct BwdLayout {
+    int64_t chunks_ub;
+    size_t table_off, ckpt_off, part_off, total;
+};
+static BwdLayout bwd_layout(const kda_desc* d) {
+    BwdLayout L;
+    L.chunks_ub = (d->total_tokens + kChunk - 1) / kChunk + d->num_seqs;
+    L.table_off = sizeof(DeviceHeader);
+    L.ckpt_off = align_up(L.table_off + ((size_t)d->num_seqs + 1) * sizeof(int32_t), 1024);
+    L.part_off = align_up(L.ckpt_off + backward_ckpt_bytes(d->d_k, d->num_heads, L.chunks_ub), 1024);
+    L.total = L.part_off + backward_part_bytes(d->d_k, d->num_heads, d->total_tokens);
+    return L;
+}
+
+size_t kda_backward_workspace_bytes(const kda_desc* d) {
+    if (!desc_ok(d) || !shape_supported(d)) return 0;
+    return bwd_layout(d).total;
+}
+
+int kda_prefill_backward(const kda_desc* d, const void* q, const void* k, const void* v,
+                         const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
+                         const float* initial_state, const void* d_out, const float* d_final_state, float* dq,
+                         float* dk, float* dv, float* dlog_alpha, float* dbeta, float* d_initial_state,
+                         kda_stream_t stream) {
+    if (!desc_ok(d)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!shape_supported(d)) return KDA_ERR_UNSUPPORTED;
+    const int N = d->num_seqs, H = d->num_heads, D = d->d_k;
+    const int64_t T = d->total_tokens;
+    if (cu_seqlens == nullptr && N != 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (N == 0) return KDA_OK;
+    const size_t esz = d->dtype == KDA_BF16 ? 2 : 4;
+    const bool scalar_gate = (d->flags & KDA_FLAG_SCALAR_GATE) != 0;
+    const size_t nqk = (size_t)T * H * D * esz, nb = (size_t)T * H * esz, nla = scalar_gate ? nb : nqk;
+    const size_t g_qk = (size_t)T * H * D * 4, g_b = (size_t)T * H * 4, g_la = scalar_gate ? g_b : g_qk;
+    const size_t nstate = (size_t)N * H * D * D * sizeof(float);
+    if (T > 0) {
+        if (!q || !k || !v || !log_alpha || !beta || !d_out || !dq || !dk || !dv || !dlog_alpha || !dbeta)
+            return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_out) ||
+            (scalar_gate ? ((uintptr_t)log_alpha % esz) != 0 : !aligned16(log_alpha)) || ((uintptr_t)beta % esz))
+            return KDA_ERR_INVALID_ARGUMENT;
+        if (((uintptr_t)dq | (uintptr_t)dk | (uintptr_t)dv | (uintptr_t)dlog_alpha | (uintptr_t)dbeta) & 3u)
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if ((cu_seqlens && !aligned16(cu_seqlens)) || (initial_state && !aligned16(initial_state)) ||
+        (d_final_state && !aligned16(d_final_state)) || (d_initial_state && !aligned16(d_initial_state)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    // outputs may not overlap inputs or one another
+    const void* outs[6] = {dq, dk, dv, dlog_alpha, dbeta, d_initial_state};
+    const size_t osz[6] = {g_qk, g_qk, g_qk, g_la, g_b, nstate};
+    const void* ins[9] = {q, k, v, log_alpha, beta, d_out, initial_state, d_final_state, cu_seqlens};
+    const size_t isz[9] = {nqk, nqk, nqk, nla, nb, nqk, nstate, nstate, ((size_t)N + 1) * 4};
+    for (int a = 0; a < 6; ++a) {
+        for (int b = 0; b < 9; ++b)
+            if (overlaps(outs[a], osz[a], ins[b], isz[b])) return KDA_ERR_INVALID_ARGUMENT;
+        for (int b = a + 1; b < 6; ++b)
+            if (overlaps(outs[a], osz[a], outs[b], osz[b])) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    const BwdLayout L = bwd_layout(d);
+    if (!d->workspace || d->workspace_bytes < L.total || ((uintptr_t)d->workspace & 255u)) return KDA_ERR_WORKSPACE;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = (char*)d->workspace;
+    DeviceHeader* hdr = (DeviceHeader*)ws;
+    int32_t* chunk_first = (int32_t*)(ws + L.table_off);
+    kda_sequence_table<<<1, kPrepThreads, 0, s>>>(cu_seqlens, N, T, hdr, chunk_first, L.chunks_ub);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    BackwardArgs a;
+    a.dtype = d->dtype; a.d = D; a.N = N; a.H = H; a.T = T;
+    a.q = q; a.k = k; a.v = v; a.la = log_alpha; a.beta = beta; a.dout = d_out; a.la_scalar = scalar_gate ? 1 : 0;
+    a.cu = cu_seqlens ? cu_seqlens : hdr->pad;
+    a.s0 = initial_state; a.dfinal = d_final_state;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dla = dlog_alpha; a.dbeta = dbeta; a.ds0 = d_initial_state;
+    a.hdr = hdr; a.chunk_first = chunk_first;
+    a.ckpt = (float*)(ws + L.ckpt_off); a.part = (float*)(ws + L.part_off);
+    if ((e = backward_launch(a, s)) != cudaSuccess) return cuda_fail(e);
+    return KDA_OK;
+}
+
 int kda_decode_step(const kda_desc* d, const void* q, const void* k, const void* v,
                     const void* log_alpha, const void* beta, float* state_inout, void* out,
                     kda_stream_t stream) {

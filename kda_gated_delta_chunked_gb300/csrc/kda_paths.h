@@ -37,6 +37,24 @@ struct PrefillArgs {
 
 cudaError_t prefill_launch(int path, const PrefillArgs& a, cudaStream_t stream);
 
+// Reverse mode of the prefill (kda_backward.cu).
+struct BackwardArgs {
+    int dtype, d, N, H;
+    int64_t T;
+    const void *q, *k, *v, *la, *beta, *dout;
+    int la_scalar;
+    const int32_t* cu;
+    const float *s0, *dfinal;
+    float *dq, *dk, *dv, *dla, *dbeta, *ds0;
+    void* hdr;
+    const int32_t* chunk_first;
+    float* ckpt;                 // kept states, backward_ckpt_bytes
+    float* part;                 // per-tile partial sums, backward_part_bytes
+};
+size_t backward_ckpt_bytes(int d, int H, int64_t chunks_ub);
+size_t backward_part_bytes(int d, int H, int64_t T);
+cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t stream);
+
 cudaError_t decode_step_launch(int dtype, int d, const void* q, const void* k, const void* v,
                                const void* la, int la_scalar, const void* beta, float* state, void* out,
                                int N, int H, cudaStream_t stream);

@@ -133,6 +133,26 @@ def test_snapshot_host_validation():
     assert call(0, None, None) == kda.KDA_ERR_WORKSPACE
 
 
+def test_backward_host_validation():
+    import torch
+    p = _ptrs(n=16)
+    q, k, v, la, b, cu, s0, do, dfin, dq, dk, dv, dla, db, ds0, ws = p
+    d = kda.make_desc(2, 4, 128, 128, 256, torch.bfloat16)
+    call = lambda **kw: kda.kda_prefill_backward(d, *[kw.get(n, x) for n, x in zip(
+        ["q", "k", "v", "la", "b", "cu", "s0", "do", "dfin", "dq", "dk", "dv", "dla", "db", "ds0"], p[:15])], 0)
+    assert kda.kda_backward_workspace_bytes(d) > 0
+    assert call() == kda.KDA_ERR_WORKSPACE                               # arguments fine, no workspace
+    assert call(do=None) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert call(dbeta=None, db=None) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert call(dq=_FakePtr(dq.addr + 2)) == kda.KDA_ERR_INVALID_ARGUMENT  # 4-byte gradients
+    assert call(ds0=_FakePtr(ds0.addr + 4)) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert call(dk=_FakePtr(q.addr + 64)) == kda.KDA_ERR_INVALID_ARGUMENT  # output over an input
+    assert call(dv=_FakePtr(dk.addr + 64)) == kda.KDA_ERR_INVALID_ARGUMENT  # two outputs overlap
+    assert call(ds0=None, dfin=None) == kda.KDA_ERR_WORKSPACE
+    bad = kda.make_desc(2, 4, 96, 96, 256, torch.bfloat16)
+    assert kda.kda_prefill_backward(bad, *p[:15], 0) == kda.KDA_ERR_UNSUPPORTED
+
+
 def test_decode_host_validation():
     import torch
     q, k, v, la, b, st, out = _ptrs(n=7)
