@@ -295,7 +295,7 @@ static BwdLayout bwd_layout(const kda_desc* d) {
     L.table_off = sizeof(DeviceHeader);
     L.ckpt_off = align_up(L.table_off + ((size_t)d->num_seqs + 1) * sizeof(int32_t), 1024);
     L.part_off = align_up(L.ckpt_off + backward_ckpt_bytes(d->d_k, d->num_heads, L.chunks_ub), 1024);
-    L.total = L.part_off + backward_part_bytes(d->d_k, d->num_heads, d->total_tokens);
+    L.total = L.part_off + backward_part_bytes(d->num_seqs, d->d_k, d->num_heads, d->total_tokens);
     return L;
 }
 

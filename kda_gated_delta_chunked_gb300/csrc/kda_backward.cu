@@ -12,8 +12,9 @@
 //           dk_t = beta_t dS e - S' de;      dS' = dS - k_t de^T
 //   decay:  dlog_alpha_t = alpha_t o rowsum(dS' o S_{t-1});     dS <- Diag(alpha_t) dS'
 //
-// Columns of S (and of dS) never mix, so a CTA owns a 32-column tile of one
-// (sequence, head) and walks the whole sequence: first forward, keeping the
+// Columns of S (and of dS) never mix, so a CTA owns a tile of 16 or 32 state
+// columns of one (sequence, head) (16 when that is needed to give every SM a
+// CTA) and walks the whole sequence: first forward, keeping the
 // tile's state every kBlk tokens in the workspace, then backwards block by
 // block, recomputing the block's states into shared memory and applying the
 // rules above.  dv and the initial-state gradient belong to the tile; dq, dk,
@@ -25,23 +26,38 @@
 
 namespace kda {
 
-constexpr int kBwdCols = 32;        // state columns per CTA
-constexpr int kBwdThreads = 256;    // 8 row groups x 32 columns
+constexpr int kBwdThreads = 256;    // (256 / COLS) row groups x COLS columns
 constexpr int kBlk = 8;             // tokens between kept states
 
-template <int D> struct BwdSmem {
-    static constexpr int kRP = D / 8;                 // rows per thread
-    float st[kBlk][D][kBwdCols];                      // S_{t-1} of each token of the block
+// Thread (rg, j) = (tid % RG, tid / RG): the RG row groups of a column sit in
+// one warp, so sums over rows are warp shuffles; sums over the tile's columns
+// combine the warp's columns by shuffles and the 8 warps through red[].
+template <int D, int COLS> struct BwdSmem {
+    static constexpr int kRG = kBwdThreads / COLS;    // row groups (16 or 8: a power of two <= 32)
+    static constexpr int kRP = D / kRG;               // rows per thread
+    float st[kBlk][D][COLS];                          // S_{t-1} of each token of the block
     float k[kBlk][D], q[kBlk][D], alpha[kBlk][D];
-    float e[kBlk][kBwdCols], v[kBlk][kBwdCols], dout[kBlk][kBwdCols];
+    float e[kBlk][COLS], v[kBlk][COLS], dout[kBlk][COLS];
     float beta[kBlk];
-    float red_rows[8][kBwdCols];                      // per-row-group partial column sums
-    float red_cols[3][D][kBwdCols + 1];               // per-column partials of dq, dk, dalpha
+    float red[2][kBwdThreads / 32][3 * D + 1];        // per-warp column sums (dq, dk, dalpha, dbeta), 2 buffers
 };
 
+// Sum over the RG lanes of a column (aligned lane groups of a warp).
+template <int RG> __device__ __forceinline__ float rows_sum(float x) {
+#pragma unroll
+    for (int o = RG / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+// Sum over the warp's columns (lanes RG apart).
+template <int RG> __device__ __forceinline__ float warp_cols_sum(float x) {
+#pragma unroll
+    for (int o = RG; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
 // Loads the per-token inputs of tokens [t, t + n) of head h into shared memory.
-template <typename T, int D>
-__device__ __forceinline__ void bwd_load_tokens(BwdSmem<D>& sm, int64_t t, int n, int h, int H, int col0,
+template <typename T, int D, int COLS>
+__device__ __forceinline__ void bwd_load_tokens(BwdSmem<D, COLS>& sm, int64_t t, int n, int h, int H, int col0,
                                                 const T* q, const T* k, const T* v, const T* la, int la_scalar,
                                                 const T* beta, const T* dout) {
     for (int e = threadIdx.x; e < n * D; e += kBwdThreads) {
@@ -51,8 +67,8 @@ __device__ __forceinline__ void bwd_load_tokens(BwdSmem<D>& sm, int64_t t, int n
         sm.q[r][i] = to_f32(q[gi]);
         sm.alpha[r][i] = expf(to_f32(la[la_scalar ? (size_t)(t + r) * H + h : gi]));
     }
-    for (int e = threadIdx.x; e < n * kBwdCols; e += kBwdThreads) {
-        const int r = e / kBwdCols, j = e % kBwdCols;
+    for (int e = threadIdx.x; e < n * COLS; e += kBwdThreads) {
+        const int r = e / COLS, j = e % COLS;
         const size_t gi = ((size_t)(t + r) * H + h) * D + col0 + j;
         sm.v[r][j] = to_f32(v[gi]);
         sm.dout[r][j] = to_f32(dout[gi]);
@@ -60,11 +76,15 @@ __device__ __forceinline__ void bwd_load_tokens(BwdSmem<D>& sm, int64_t t, int n
     if (threadIdx.x < n) sm.beta[threadIdx.x] = to_f32(beta[(size_t)(t + threadIdx.x) * H + h]);
 }
 
-// One forward step on the thread's rows of column j: S <- S' + beta k e^T,
-// with the column sum over row groups through red_rows.  Returns e_j.
-template <int D>
-__device__ __forceinline__ float bwd_fwd_step(BwdSmem<D>& sm, float (&S)[D / 8], int r, int rg, int j) {
-    constexpr int RP = D / 8;
+// True on the lanes of a warp's first column (they hold the warp's column sums).
+__device__ __forceinline__ bool lane_col0(int tid, int RG) { return (tid & 31) < RG; }
+
+// One forward step on the thread's rows of column j: S <- S' + beta k e^T.
+// Returns e_j.
+template <int D, int COLS>
+__device__ __forceinline__ float bwd_fwd_step(const BwdSmem<D, COLS>& sm, float (&S)[BwdSmem<D, COLS>::kRP],
+                                              int r, int rg, int j) {
+    constexpr int RP = BwdSmem<D, COLS>::kRP, RG = BwdSmem<D, COLS>::kRG;
     float pk = 0.f;
 #pragma unroll
     for (int a = 0; a < RP; ++a) {
@@ -72,20 +92,14 @@ __device__ __forceinline__ float bwd_fwd_step(BwdSmem<D>& sm, float (&S)[D / 8],
         S[a] *= sm.alpha[r][i];
         pk = fmaf(sm.k[r][i], S[a], pk);
     }
-    sm.red_rows[rg][j] = pk;
-    __syncthreads();
-    float pred = 0.f;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) pred += sm.red_rows[g][j];
-    const float e = sm.v[r][j] - pred;
+    const float e = sm.v[r][j] - rows_sum<RG>(pk);
     const float be = sm.beta[r] * e;
 #pragma unroll
     for (int a = 0; a < RP; ++a) S[a] = fmaf(sm.k[r][rg * RP + a], be, S[a]);
-    __syncthreads();                                   // red_rows free again
     return e;
 }
 
-template <typename T, int D>
+template <typename T, int D, int COLS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const T* __restrict__ la, int la_scalar, const T* __restrict__ beta,
@@ -94,19 +108,20 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
                   const float* __restrict__ s0, const T* __restrict__ dout, const float* __restrict__ dfinal,
                   float* __restrict__ ckpt, float* __restrict__ part, float* __restrict__ dv,
                   float* __restrict__ ds0) {
-    constexpr int RP = D / 8;
-    constexpr int kTiles = D / kBwdCols;
+    using SM = BwdSmem<D, COLS>;
+    constexpr int RP = SM::kRP, RG = SM::kRG;
+    constexpr int kTiles = D / COLS;
     if (hdr->status != KDA_OK) return;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
+    SM& sm = *reinterpret_cast<SM*>(smem_raw);
     const int nh = blockIdx.x, tile = blockIdx.y, n = nh / H, h = nh % H;
-    const int col0 = tile * kBwdCols;
-    const int tid = threadIdx.x, rg = tid >> 5, j = tid & 31;
+    const int col0 = tile * COLS;
+    const int tid = threadIdx.x, rg = tid % RG, j = tid / RG, warp = tid >> 5;
     const int64_t t0 = cu[n];
     const int L = (int)(cu[n + 1] - t0);
     // kept states: block b of this sequence at ckpt[((blk0 + b) * H + h) * kTiles + tile]
     const int64_t blk0 = (int64_t)chunk_first[n] * (kChunk / kBlk);
-    auto kept = [&](int b) { return ckpt + (((size_t)(blk0 + b) * H + h) * kTiles + tile) * (size_t)D * kBwdCols; };
+    auto kept = [&](int b) { return ckpt + (((size_t)(blk0 + b) * H + h) * kTiles + tile) * (size_t)D * COLS; };
     const size_t sbase = (size_t)nh * D * D;
 
     // ---- forward: keep the state at the start of every block
@@ -116,12 +131,13 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     for (int b = 0; b * kBlk < L; ++b) {
         float* kp = kept(b);
 #pragma unroll
-        for (int a = 0; a < RP; ++a) kp[(rg * RP + a) * kBwdCols + j] = S[a];
+        for (int a = 0; a < RP; ++a) kp[(rg * RP + a) * COLS + j] = S[a];
         const int n_b = min(kBlk, L - b * kBlk);
         __syncthreads();
-        bwd_load_tokens<T, D>(sm, t0 + (int64_t)b * kBlk, n_b, h, H, col0, q, k, v, la, la_scalar, beta, dout);
+        bwd_load_tokens<T, D, COLS>(sm, t0 + (int64_t)b * kBlk, n_b, h, H, col0, q, k, v, la, la_scalar, beta,
+                                    dout);
         __syncthreads();
-        for (int r = 0; r < n_b; ++r) bwd_fwd_step<D>(sm, S, r, rg, j);
+        for (int r = 0; r < n_b; ++r) bwd_fwd_step<D, COLS>(sm, S, r, rg, j);
     }
 
     // ---- backward, block by block from the end
@@ -133,20 +149,21 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         const int n_b = min(kBlk, L - b * kBlk);
         const int64_t tb = t0 + (int64_t)b * kBlk;
         __syncthreads();
-        bwd_load_tokens<T, D>(sm, tb, n_b, h, H, col0, q, k, v, la, la_scalar, beta, dout);
+        bwd_load_tokens<T, D, COLS>(sm, tb, n_b, h, H, col0, q, k, v, la, la_scalar, beta, dout);
         const float* kp = kept(b);
 #pragma unroll
-        for (int a = 0; a < RP; ++a) S[a] = kp[(rg * RP + a) * kBwdCols + j];
+        for (int a = 0; a < RP; ++a) S[a] = kp[(rg * RP + a) * COLS + j];
         __syncthreads();
         // recompute the block: st[r] = S_{t-1} of token r, e[r]
         for (int r = 0; r < n_b; ++r) {
 #pragma unroll
             for (int a = 0; a < RP; ++a) sm.st[r][rg * RP + a][j] = S[a];
-            const float e = bwd_fwd_step<D>(sm, S, r, rg, j);
+            const float e = bwd_fwd_step<D, COLS>(sm, S, r, rg, j);
             if (rg == 0) sm.e[r][j] = e;
         }
         __syncthreads();
         for (int r = n_b - 1; r >= 0; --r) {
+            float (&red)[3 * D + 1] = sm.red[r & 1][warp];
             const int64_t t = tb + r;
             const float bt = sm.beta[r], e_j = sm.e[r][j], do_j = sm.dout[r][j];
             float Sp[RP], Sprev[RP];
@@ -163,11 +180,7 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
                 dS[a] = fmaf(sm.q[r][i], do_j, dS[a]);
                 uk = fmaf(sm.k[r][i], dS[a], uk);
             }
-            sm.red_rows[rg][j] = uk;
-            __syncthreads();
-            float u = 0.f;
-#pragma unroll
-            for (int g = 0; g < 8; ++g) u += sm.red_rows[g][j];
+            const float u = rows_sum<RG>(uk);
             const float de = bt * u;
             if (rg == 0) dv[((size_t)t * H + h) * D + col0 + j] = de;
             // write and decay
@@ -179,33 +192,30 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
                 pa[a] = dSp * Sprev[a];
                 dS[a] = sm.alpha[r][i] * dSp;
             }
-            // column sums of dq, dk, dalpha over the tile: transpose through shared memory
+            // column sums over the tile of dq, dk, dalpha and dbeta (= e . u):
+            // the warp's columns by shuffles, then the 8 warps through red[]
 #pragma unroll
             for (int a = 0; a < RP; ++a) {
-                const int i = rg * RP + a;
-                sm.red_cols[0][i][j] = pq[a];
-                sm.red_cols[1][i][j] = pk[a];
-                sm.red_cols[2][i][j] = pa[a];
+                const float sq = warp_cols_sum<RG>(pq[a]);
+                const float sk = warp_cols_sum<RG>(pk[a]);
+                const float sa = warp_cols_sum<RG>(pa[a]);
+                if (lane_col0(tid, RG)) {
+                    const int i = rg * RP + a;
+                    red[i] = sq;
+                    red[D + i] = sk;
+                    red[2 * D + i] = sa;
+                }
             }
+            const float eu = warp_cols_sum<RG>(rg == 0 ? e_j * u : 0.f);
+            if ((tid & 31) == 0) red[3 * D] = eu;
             __syncthreads();
-            // dbeta partial = e . u over the tile (u_j of every column is in red_rows)
             float* pt = part + ((size_t)tile * T_tot + t) * H * (3 * D + 1) + (size_t)h * (3 * D + 1);
-            for (int w = tid; w < 3 * D; w += kBwdThreads) {
-                const int m = w / D, i = w % D;
+            for (int w = tid; w <= 3 * D; w += kBwdThreads) {
                 float acc = 0.f;
-#pragma unroll 8
-                for (int c = 0; c < kBwdCols; ++c) acc += sm.red_cols[m][i][c];
-                pt[w] = m == 2 ? acc * sm.alpha[r][i] : acc;
-            }
-            if (tid < 32) {
-                float eu = 0.f;
-                for (int g = 0; g < 8; ++g) eu += sm.red_rows[g][tid];   // u of column tid
-                eu *= sm.e[r][tid];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) eu += __shfl_xor_sync(0xffffffffu, eu, o);
-                if (tid == 0) pt[3 * D] = eu;
+                for (int g = 0; g < kBwdThreads / 32; ++g) acc += sm.red[r & 1][g][w];
+                pt[w] = (w >= 2 * D && w < 3 * D) ? acc * sm.alpha[r][w - 2 * D] : acc;
             }
-            __syncthreads();
         }
     }
     if (ds0) {
@@ -219,9 +229,8 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
 template <int D>
 __global__ void __launch_bounds__(256)
 kda_backward_reduce(const float* __restrict__ part, const DeviceHeader* __restrict__ hdr, int64_t T_tot, int H,
-                    int la_scalar, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dla,
-                    float* __restrict__ dbeta) {
-    constexpr int kTiles = D / kBwdCols;
+                    int kTiles, int la_scalar, float* __restrict__ dq, float* __restrict__ dk,
+                    float* __restrict__ dla, float* __restrict__ dbeta) {
     constexpr int W = 3 * D + 1;
     if (hdr->status != KDA_OK) return;
     const int64_t th = blockIdx.x;                    // (token, head)
@@ -252,33 +261,42 @@ kda_backward_reduce(const float* __restrict__ part, const DeviceHeader* __restri
 size_t backward_ckpt_bytes(int d, int H, int64_t chunks_ub) {
     return (size_t)chunks_ub * (kChunk / kBlk) * H * (size_t)d * d * sizeof(float);
 }
-size_t backward_part_bytes(int d, int H, int64_t T) {
-    return (size_t)(d / kBwdCols) * T * H * (3 * (size_t)d + 1) * sizeof(float);
+// Columns per CTA: 16 when 32-column tiles would leave SMs idle.
+static int bwd_cols(int N, int H, int d) { return (int64_t)N * H * (d / 32) < 152 ? 16 : 32; }
+
+size_t backward_part_bytes(int N, int d, int H, int64_t T) {
+    return (size_t)(d / bwd_cols(N, H, d)) * T * H * (3 * (size_t)d + 1) * sizeof(float);
 }
 
-template <typename T, int D>
+template <typename T, int D, int COLS>
 static cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t stream) {
     cudaError_t e;
-    const size_t smem = sizeof(BwdSmem<D>);
-    if ((e = cudaFuncSetAttribute(kda_backward_tile<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-        cudaSuccess) return e;
-    kda_backward_tile<T, D><<<dim3((unsigned)a.N * a.H, D / kBwdCols), kBwdThreads, smem, stream>>>(
+    const size_t smem = sizeof(BwdSmem<D, COLS>);
+    if ((e = cudaFuncSetAttribute(kda_backward_tile<T, D, COLS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)) != cudaSuccess) return e;
+    kda_backward_tile<T, D, COLS><<<dim3((unsigned)a.N * a.H, D / COLS), kBwdThreads, smem, stream>>>(
         (const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.la, a.la_scalar, (const T*)a.beta, a.cu,
         (const DeviceHeader*)a.hdr, a.chunk_first, a.H, a.T, a.s0, (const T*)a.dout, a.dfinal, a.ckpt, a.part,
         a.dv, a.ds0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.T > 0) {
         kda_backward_reduce<D><<<(unsigned)(a.T * a.H), 256, 0, stream>>>(
-            a.part, (const DeviceHeader*)a.hdr, a.T, a.H, a.la_scalar, a.dq, a.dk, a.dla, a.dbeta);
+            a.part, (const DeviceHeader*)a.hdr, a.T, a.H, D / COLS, a.la_scalar, a.dq, a.dk, a.dla, a.dbeta);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
+template <typename T, int D>
+static cudaError_t launch_bwd_cols(const BackwardArgs& a, cudaStream_t stream) {
+    return bwd_cols(a.N, a.H, D) == 16 ? launch_bwd<T, D, 16>(a, stream) : launch_bwd<T, D, 32>(a, stream);
+}
+
 cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t stream) {
     if (a.dtype == KDA_BF16)
-        return a.d == 128 ? launch_bwd<__nv_bfloat16, 128>(a, stream) : launch_bwd<__nv_bfloat16, 64>(a, stream);
-    return a.d == 128 ? launch_bwd<float, 128>(a, stream) : launch_bwd<float, 64>(a, stream);
+        return a.d == 128 ? launch_bwd_cols<__nv_bfloat16, 128>(a, stream)
+                          : launch_bwd_cols<__nv_bfloat16, 64>(a, stream);
+    return a.d == 128 ? launch_bwd_cols<float, 128>(a, stream) : launch_bwd_cols<float, 64>(a, stream);
 }
 
 }  // namespace kda

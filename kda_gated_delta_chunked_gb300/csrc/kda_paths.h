@@ -52,7 +52,7 @@ struct BackwardArgs {
     float* part;                 // per-tile partial sums, backward_part_bytes
 };
 size_t backward_ckpt_bytes(int d, int H, int64_t chunks_ub);
-size_t backward_part_bytes(int d, int H, int64_t T);
+size_t backward_part_bytes(int N, int d, int H, int64_t T);
 cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t stream);
 
 cudaError_t decode_step_launch(int dtype, int d, const void* q, const void* k, const void* v,

@@ -64,6 +64,7 @@
 // Every wait on an mbarrier is bounded; on timeout the kernel records
 // KDA_ERR_TIMEOUT in the device status word, drains its own copies and exits.
 #include <cudaTypedefs.h>
+#include <string.h>
 
 #include "kda_common.cuh"
 #include "kda_paths.h"
@@ -114,7 +115,7 @@ struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per 
     static constexpr uint32_t kY = 65536;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB
     static constexpr uint32_t kPart = 65536;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
     static constexpr uint32_t kGS = 49152;      // (slow path, before A^) g, fp32 [64][128], 32 KB
-    static constexpr uint32_t kMisc = 81920;    // beta[64], Em[128], barriers, TMEM slot, flags
+    static constexpr uint32_t kMisc = 81920;    // beta[64], Em[128], barriers, TMEM slot, flags, g_C, g_0
     static constexpr uint32_t kBytes = kMisc + 2048 + 1024;
 };
 
@@ -217,6 +218,8 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     uint64_t* bars = (uint64_t*)(sm + SmemA::kMisc + 768);       // [0] V tile, [1] MMAs
     uint32_t* s_tmem = (uint32_t*)(sm + SmemA::kMisc + 800);
     int* s_flag = (int*)(sm + SmemA::kMisc + 816);                // [0] slow path, [1] abort
+    float* s_gtot = (float*)(sm + SmemA::kMisc + 1024);           // [128] g_C per channel
+    float* s_g0 = (float*)(sm + SmemA::kMisc + 1536);             // [128] g of the first token
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, h = blockIdx.y;
@@ -279,40 +282,43 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         float4* part = (float4*)(sm + SmemA::kPart) + (R * kTcD + 8 * C) / 4;
         part[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
         part[1] = make_float4(s8[4], s8[5], s8[6], s8[7]);
+        if (R == 0) {                                   // g of the chunk's first token
+            float4* g0 = (float4*)(s_g0 + 8 * C);
+            g0[0] = make_float4(gl[0][0], gl[0][1], gl[0][2], gl[0][3]);
+            g0[1] = make_float4(gl[0][4], gl[0][5], gl[0][6], gl[0][7]);
+        }
     }
     __syncthreads();
-    // Prefix over the 16 row groups: g before this thread's rows, at row 31 (g_m)
-    // and at row 63 (g_C), for its 8 channels.
-    float gbase[8], gm[8], gC[8];
-    {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const float4* part = (const float4*)(sm + SmemA::kPart);
-#pragma unroll 4
-        for (int rg = 0; rg < 16; ++rg) {
-            if (rg == R) {
+    // Exclusive prefix over the 16 row groups, one thread per channel, in place;
+    // the chunk total g_C goes to s_gtot.  A chunk whose decay spans more than
+    // 2^kMaxSpanLog2 in some channel takes the slow path.
+    if (tid < kTcD) {
+        float* pc = (float*)(sm + SmemA::kPart) + tid;
+        float x[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gbase[e] = acc[e];
-            }
-            if (rg == 8) {
+        for (int rg = 0; rg < 16; ++rg) x[rg] = pc[rg * kTcD];
+        float acc = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gm[e] = acc[e];
-            }
-            const float4 a = part[(rg * kTcD + 8 * C) / 4], b = part[(rg * kTcD + 8 * C) / 4 + 1];
-            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) gC[e] = acc[e];
-        if (R == 0) {
-            bool wide = false;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) wide |= (gl[0][e] - gC[e] > kMaxSpanLog2);
-            if (wide) s_flag[0] = 1;                    // any writer sets 1
-        }
+        for (int rg = 0; rg < 16; ++rg) { pc[rg * kTcD] = acc; acc += x[rg]; }
+        s_gtot[tid] = acc;
+        if (s_g0[tid] - acc > kMaxSpanLog2) s_flag[0] = 1;   // any writer sets 1
     }
     tc_fence_before_sync();
-    __syncthreads();                                    // also: kPart no longer read
+    __syncthreads();
     tc_fence_after_sync();
+    // g before this thread's rows, at row 31 (g_m) and at row 63 (g_C), for its 8 channels.
+    float gbase[8], gm[8], gC[8];
+    {
+        const float4* part = (const float4*)(sm + SmemA::kPart);
+        const float4* tot = (const float4*)s_gtot;
+        const float4 a = part[(R * kTcD + 8 * C) / 4], b = part[(R * kTcD + 8 * C) / 4 + 1];
+        const float4 c = part[(8 * kTcD + 8 * C) / 4], d = part[(8 * kTcD + 8 * C) / 4 + 1];
+        const float4 e = tot[2 * C], f = tot[2 * C + 1];
+        gbase[0] = a.x; gbase[1] = a.y; gbase[2] = a.z; gbase[3] = a.w;
+        gbase[4] = b.x; gbase[5] = b.y; gbase[6] = b.z; gbase[7] = b.w;
+        gm[0] = c.x; gm[1] = c.y; gm[2] = c.z; gm[3] = c.w; gm[4] = d.x; gm[5] = d.y; gm[6] = d.z; gm[7] = d.w;
+        gC[0] = e.x; gC[1] = e.y; gC[2] = e.z; gC[3] = e.w; gC[4] = f.x; gC[5] = f.y; gC[6] = f.z; gC[7] = f.w;
+    }
     const uint32_t tmem = *s_tmem;
     const bool slow = s_flag[0] != 0;
     if (slow) {
@@ -623,6 +629,8 @@ __device__ __forceinline__ uint32_t mn_off(uint32_t row, uint32_t col, uint32_t 
 
 // Arguments shared by the chain launches.
 struct ChainArgs {
+    CUtensorMap tm_out;          // out [T, H, 128] bf16, box 16 columns x 1 head x 64 tokens
+    int has_tm_out;
     const int32_t* cu;
     DeviceHeader* hdr;
     const int32_t* chunk_first;
@@ -809,7 +817,11 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
             } else if (kOut) {
                 // O = O0 + Q' S -> out.  The TMEM loads are warp-collective: every
                 // lane takes part, only the stores of real tokens are predicated.
+                // A full chunk's O goes back into the stage's O0 tiles (same layout
+                // as a [64 x 16] box of out) and leaves with TMA stores; a partial
+                // last chunk is stored row by row.
                 const int64_t t = seq0 + (int64_t)(cb + it) * kChunk + tok;
+                const bool full = A.has_tm_out && seq0 + (int64_t)(cb + it + 1) * kChunk <= seq1;
                 const bool store = good && t < seq1;
 #pragma unroll
                 for (int j2 = 0; j2 < kCols; j2 += 16 * kLdB) {
@@ -827,17 +839,29 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                     unpack8(*(const uint4*)(o0 + 16), b);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) { a[e] += d[e]; b[e] += d[8 + e]; }
-                    if (store) {
+                    if (full) {
+                        uint4* dst = (uint4*)(st + L::kO0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2));
+                        dst[0] = pack8(a);
+                        dst[1] = pack8(b);
+                    } else if (store) {
                         uint4* dst = (uint4*)(out + ((size_t)t * H + h) * kTcD + c);
                         dst[0] = pack8(a);
                         dst[1] = pack8(b);
                     }
                   }
                 }
+                if (full) fence_proxy_async_smem();
             }
             tc_fence_before_sync();
             if (!bar_and(32 * kChainWarps, good)) { ok = false; break; }
             tc_fence_after_sync();
+            if (kOut && tid == 0 && A.has_tm_out && seq0 + (int64_t)(cb + it + 1) * kChunk <= seq1) {
+#pragma unroll
+                for (int tl = 0; tl < kTcD / kTile; ++tl)
+                    tma_store_3d(&A.tm_out, st + L::kO0 + tl * TcRec::kTileBytes, tl * kTile, h,
+                                 (int)(seq0 + (int64_t)(cb + it) * kChunk));
+                bulk_commit();
+            }
             if (tid == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -869,6 +893,7 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
             fence_proxy_async_smem();
             tc_fence_before_sync();
             ok = bar_and(32 * kChainWarps, good);
+            if (kOut && tid == 0) bulk_wait_read_all();        // the stage's O tiles have been stored
             if (ok && tid == 0) mbar_arrive(&empty[s]);
         }
         if (!ok) {
@@ -898,14 +923,14 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
 
 // Launch 1: segment 0's output pass (blockIdx.y == 0) beside the transition
 // passes of segments 1 .. segs-2 (blockIdx.y = p).
-__global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_first(const ChainArgs A) {
+__global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_first(const __grid_constant__ ChainArgs A) {
     if (A.hdr->status != KDA_OK) return;
     if (blockIdx.y == 0) chain_segment<128>(A, 0);
     else chain_segment<256>(A, blockIdx.y);
 }
 
 // Launch 3: the output passes of segments 1 .. segs-1 (p = blockIdx.y + 1).
-__global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_rest(const ChainArgs A) {
+__global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_rest(const __grid_constant__ ChainArgs A) {
     if (A.hdr->status != KDA_OK) return;
     chain_segment<128>(A, blockIdx.y + 1);
 }
@@ -970,6 +995,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // V [T, H, 128] bf16; box = 64 tokens x 64 channels of one head, 128-byte
 // swizzle (the MN-major operand layout of the second intra-chunk product).
+// out [T, H, 128] bf16; box = 16 channels x 1 head x 64 tokens, no swizzle
+// (the layout of a U0 / O0 record tile).
+static bool make_out_map(CUtensorMap* m, void* base, int64_t T, int H) {
+    auto enc = encode_fn();
+    if (!enc || T <= 0) return false;
+    cuuint64_t gdim[3] = {(cuuint64_t)kTcD, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t gstr[2] = {(cuuint64_t)kTcD * 2, (cuuint64_t)H * kTcD * 2};
+    cuuint32_t box[3] = {kTile, 1, kChunk}, es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static bool make_v_map(CUtensorMap* m, const void* base, int64_t T, int H) {
     auto enc = encode_fn();
     if (!enc) return false;
@@ -1002,6 +1040,8 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[1], stream)) != cudaSuccess) return e;
     const ScanPlan plan = scan_plan(a.N, a.H, T);
     ChainArgs ca;
+    memset(&ca, 0, sizeof(ca));
+    ca.has_tm_out = make_out_map(&ca.tm_out, a.out, T, a.H) ? 1 : 0;
     ca.cu = a.cu; ca.hdr = (DeviceHeader*)a.hdr; ca.chunk_first = a.chunk_first; ca.H = a.H;
     ca.len0 = plan.len0; ca.len = plan.len; ca.segs_max = plan.segs_max;
     ca.recs = (const uint8_t*)a.recs; ca.initial_state = a.s0; ca.out = (__nv_bfloat16*)a.out;
