@@ -29,13 +29,15 @@ namespace kda {
 constexpr int kBwdThreads = 256;    // (256 / COLS) row groups x COLS columns
 constexpr int kBlk = 8;             // tokens between kept states
 
-// Thread (rg, j) = (tid % RG, tid / RG): the RG row groups of a column sit in
-// one warp, so sums over rows are warp shuffles; sums over the tile's columns
-// combine the warp's columns by shuffles and the 8 warps through red[].
+// Thread (rg, j) = (tid % RG, tid / RG) owns rows i = a * RG + rg (a < RP) of
+// column j: the RG row groups of a column sit in one warp, so sums over rows
+// are warp shuffles, and neighbouring lanes touch neighbouring rows (shared
+// memory without bank conflicts); sums over the tile's columns combine the
+// warp's columns by shuffles and the 8 warps through red[].
 template <int D, int COLS> struct BwdSmem {
     static constexpr int kRG = kBwdThreads / COLS;    // row groups (16 or 8: a power of two <= 32)
     static constexpr int kRP = D / kRG;               // rows per thread
-    float st[kBlk][D][COLS];                          // S_{t-1} of each token of the block
+    float st[kBlk][kRP][COLS][kRG];                   // S_{t-1} of each token of the block, [.][a][j][rg]
     float k[kBlk][D], q[kBlk][D], alpha[kBlk][D];
     float e[kBlk][COLS], v[kBlk][COLS], dout[kBlk][COLS];
     float beta[kBlk];
@@ -88,14 +90,14 @@ __device__ __forceinline__ float bwd_fwd_step(const BwdSmem<D, COLS>& sm, float 
     float pk = 0.f;
 #pragma unroll
     for (int a = 0; a < RP; ++a) {
-        const int i = rg * RP + a;
+        const int i = a * RG + rg;
         S[a] *= sm.alpha[r][i];
         pk = fmaf(sm.k[r][i], S[a], pk);
     }
     const float e = sm.v[r][j] - rows_sum<RG>(pk);
     const float be = sm.beta[r] * e;
 #pragma unroll
-    for (int a = 0; a < RP; ++a) S[a] = fmaf(sm.k[r][rg * RP + a], be, S[a]);
+    for (int a = 0; a < RP; ++a) S[a] = fmaf(sm.k[r][a * RG + rg], be, S[a]);
     return e;
 }
 
@@ -127,11 +129,11 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     // ---- forward: keep the state at the start of every block
     float S[RP];
 #pragma unroll
-    for (int a = 0; a < RP; ++a) S[a] = s0 ? s0[sbase + (size_t)(rg * RP + a) * D + col0 + j] : 0.f;
+    for (int a = 0; a < RP; ++a) S[a] = s0 ? s0[sbase + (size_t)(a * RG + rg) * D + col0 + j] : 0.f;
     for (int b = 0; b * kBlk < L; ++b) {
         float* kp = kept(b);
 #pragma unroll
-        for (int a = 0; a < RP; ++a) kp[(rg * RP + a) * COLS + j] = S[a];
+        for (int a = 0; a < RP; ++a) kp[(a * COLS + j) * RG + rg] = S[a];
         const int n_b = min(kBlk, L - b * kBlk);
         __syncthreads();
         bwd_load_tokens<T, D, COLS>(sm, t0 + (int64_t)b * kBlk, n_b, h, H, col0, q, k, v, la, la_scalar, beta,
@@ -143,7 +145,7 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     // ---- backward, block by block from the end
     float dS[RP];
 #pragma unroll
-    for (int a = 0; a < RP; ++a) dS[a] = dfinal ? dfinal[sbase + (size_t)(rg * RP + a) * D + col0 + j] : 0.f;
+    for (int a = 0; a < RP; ++a) dS[a] = dfinal ? dfinal[sbase + (size_t)(a * RG + rg) * D + col0 + j] : 0.f;
     const int nblk = (L + kBlk - 1) / kBlk;
     for (int b = nblk - 1; b >= 0; --b) {
         const int n_b = min(kBlk, L - b * kBlk);
@@ -152,12 +154,12 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         bwd_load_tokens<T, D, COLS>(sm, tb, n_b, h, H, col0, q, k, v, la, la_scalar, beta, dout);
         const float* kp = kept(b);
 #pragma unroll
-        for (int a = 0; a < RP; ++a) S[a] = kp[(rg * RP + a) * COLS + j];
+        for (int a = 0; a < RP; ++a) S[a] = kp[(a * COLS + j) * RG + rg];
         __syncthreads();
         // recompute the block: st[r] = S_{t-1} of token r, e[r]
         for (int r = 0; r < n_b; ++r) {
 #pragma unroll
-            for (int a = 0; a < RP; ++a) sm.st[r][rg * RP + a][j] = S[a];
+            for (int a = 0; a < RP; ++a) sm.st[r][a][j][rg] = S[a];
             const float e = bwd_fwd_step<D, COLS>(sm, S, r, rg, j);
             if (rg == 0) sm.e[r][j] = e;
         }
@@ -172,8 +174,8 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
             float uk = 0.f;
 #pragma unroll
             for (int a = 0; a < RP; ++a) {
-                const int i = rg * RP + a;
-                Sprev[a] = sm.st[r][i][j];
+                const int i = a * RG + rg;
+                Sprev[a] = sm.st[r][a][j][rg];
                 Sp[a] = sm.alpha[r][i] * Sprev[a];
                 const float St = fmaf(sm.k[r][i], bt * e_j, Sp[a]);
                 pq[a] = St * do_j;
@@ -186,7 +188,7 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
             // write and decay
 #pragma unroll
             for (int a = 0; a < RP; ++a) {
-                const int i = rg * RP + a;
+                const int i = a * RG + rg;
                 pk[a] = bt * dS[a] * e_j - Sp[a] * de;
                 const float dSp = fmaf(-sm.k[r][i], de, dS[a]);
                 pa[a] = dSp * Sprev[a];
@@ -199,11 +201,10 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
                 const float sq = warp_cols_sum<RG>(pq[a]);
                 const float sk = warp_cols_sum<RG>(pk[a]);
                 const float sa = warp_cols_sum<RG>(pa[a]);
-                if (lane_col0(tid, RG)) {
-                    const int i = rg * RP + a;
-                    red[i] = sq;
-                    red[D + i] = sk;
-                    red[2 * D + i] = sa;
+                if (lane_col0(tid, RG)) {               // row a * RG + rg: consecutive lanes, consecutive words
+                    red[a * RG + rg] = sq;
+                    red[D + a * RG + rg] = sk;
+                    red[2 * D + a * RG + rg] = sa;
                 }
             }
             const float eu = warp_cols_sum<RG>(rg == 0 ? e_j * u : 0.f);
@@ -211,16 +212,17 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
             __syncthreads();
             float* pt = part + ((size_t)tile * T_tot + t) * H * (3 * D + 1) + (size_t)h * (3 * D + 1);
             for (int w = tid; w <= 3 * D; w += kBwdThreads) {
+                const int m = w / D, i = w - m * D;
                 float acc = 0.f;
 #pragma unroll
                 for (int g = 0; g < kBwdThreads / 32; ++g) acc += sm.red[r & 1][g][w];
-                pt[w] = (w >= 2 * D && w < 3 * D) ? acc * sm.alpha[r][w - 2 * D] : acc;
+                pt[w] = m == 2 ? acc * sm.alpha[r][i] : acc;
             }
         }
     }
     if (ds0) {
 #pragma unroll
-        for (int a = 0; a < RP; ++a) ds0[sbase + (size_t)(rg * RP + a) * D + col0 + j] = dS[a];
+        for (int a = 0; a < RP; ++a) ds0[sbase + (size_t)(a * RG + rg) * D + col0 + j] = dS[a];
     }
 }
 
