@@ -570,10 +570,18 @@ def cpu_baseline(w, seconds):
         t = time.perf_counter()
         oracle.prefill(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, x["initial_state"])
         spent = time.perf_counter() - t
+    # the same oracle on one core, on a sample a sixteenth as long
+    n1 = max(64, n_tok // 16)
+    x1 = prefill_inputs(w, t_range=(0, n1))
+    t = time.perf_counter()
+    oracle.prefill(x1["q"], x1["k"], x1["v"], x1["log_alpha"], x1["beta"], None, x1["initial_state"], threads=1)
+    spent1 = time.perf_counter() - t
     return {"value": round(n_tok / spent, 2), "unit": "tokens/s", "cores": oracle.default_threads(),
             "kind": "oracle", "seconds": round(spent, 2),
             "sample": f"first {n_tok} tokens x {w.num_heads} heads of {w.name} (fp64 recurrence, "
-                      f"threads over head x column block)"}
+                      f"threads over head x column block)",
+            "one_core": {"value": round(n1 / spent1, 2), "unit": "tokens/s", "cores": 1,
+                         "sample": f"first {n1} tokens x {w.num_heads} heads", "seconds": round(spent1, 2)}}
 
 
 # ----------------------------------------------------------------------------
