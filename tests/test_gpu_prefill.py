@@ -226,3 +226,41 @@ def test_segment_scan_mixed_lengths(kda):
     out, sf, _, _ = run_gpu(kda, d)
     ro, rs = run_oracle(d)
     assert_parity("segment scan, mixed", host(out), ro, host(sf), rs, "bf16")
+
+
+@pytest.mark.parametrize("case", ["no_decay", "no_write", "full_write"])
+def test_degenerate_gates(kda, case):
+    """The gates' special values: log alpha = 0 (no forgetting: DeltaNet),
+    beta = 0 (nothing written: the state only decays), beta = 1 (exact
+    overwrite along each key), on the tensor-core and CUDA-core paths."""
+    for dtype, dim in (("bf16", 128), ("f32", 64)):
+        d = prefill_inputs(custom(130, [150, 64, 1], 2, dim, dtype))
+        if case == "no_decay":
+            d["log_alpha"] = torch.zeros_like(d["log_alpha"])
+        elif case == "no_write":
+            d["beta"] = torch.zeros_like(d["beta"])
+        else:
+            d["beta"] = torch.ones_like(d["beta"])
+        out, sf, _, _ = run_gpu(kda, d)
+        ro, rs = run_oracle(d)
+        assert_parity(f"{case} {dtype} d{dim}", host(out), ro, host(sf), rs, dtype)
+        if case == "no_write":
+            # nothing written: the final state is the initial state decayed channel by channel
+            la = d["log_alpha"].double()
+            s0 = d["initial_state"].double()
+            cu = d["cu_seqlens"].tolist()
+            for n in range(len(cu) - 1):
+                decay = torch.exp(la[cu[n]:cu[n + 1]].sum(0))          # [H, d_k]
+                ref = (s0[n] * decay[:, :, None]).numpy()
+                assert np.abs(host(sf)[n] - ref).max() <= 1e-3 * max(1.0, np.abs(ref).max())
+
+
+def test_many_sequences(kda):
+    """2,500 sequences (more than one pass of the sequence-table kernel's 1,024
+    threads), lengths 0..40, including chunk-boundary lengths."""
+    lens = [(i * 7919) % 41 for i in range(2500)]
+    lens[3], lens[4], lens[5] = 64, 65, 128
+    d = prefill_inputs(custom(131, lens, 2, 128, "bf16"))
+    out, sf, _, _ = run_gpu(kda, d)
+    ro, rs = run_oracle(d)
+    assert_parity("2,500 sequences", host(out), ro, host(sf), rs, "bf16")
