@@ -190,15 +190,19 @@ def bench_workload(args):
 
 def prefill_launches(N, H, T, C=64, plan_sms=152, min_seg=128):
     """Kernels one bf16 d=128 prefill launches: the sequence table, the
-    intra-chunk kernel, then either the inter-chunk pass alone or, when a
-    sequence is long enough to be cut into segments (one per SM share, at
-    least 128 chunks each), the transition pass, the state scan and the output
-    pass."""
+    intra-chunk kernel, the first chain launch, and -- when a sequence is long
+    enough to be cut into segments -- the state scan (three or more segments)
+    and the output passes of the later segments.  Mirrors the library's plan:
+    (N * H) x (segments - 1) CTAs near the SM count, segment 0 about 1.3x the
+    others, at least 128 chunks each."""
     chunks = -(-T // C)
-    target = max(1, plan_sms // max(1, N * H))
-    seg = max(min_seg, -(-chunks // target))
-    segs = max(1, -(-chunks // seg))
-    return 2 + (3 if segs > 1 else 1)
+    target = plan_sms // max(1, N * H)
+    if target < 2 or chunks <= 2 * min_seg:
+        return 3
+    seg = max(min_seg, (10 * chunks + 10 * target + 12) // (10 * target + 13))
+    seg0 = max((13 * seg + 9) // 10, chunks - target * seg)
+    segs = 1 if chunks <= seg0 else 1 + -(-(chunks - seg0) // seg)
+    return 3 + (1 if segs > 2 else 0) + (1 if segs > 1 else 0)
 
 
 # ----------------------------------------------------------------------------
