@@ -562,6 +562,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 constexpr int kPlanSMs = 152;
 constexpr int kChainWarps = 16;                 // consumer warps (4 per TMEM lane quarter)
 constexpr int kChainThreads = 32 * kChainWarps + 32;
+constexpr int kOLeader = 64;                    // lane 0 of warp 2: issues the output pass's TMA stores
 
 struct ScanPlan {
     int len0;         // chunks of segment 0
@@ -853,23 +854,34 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                 if (full) fence_proxy_async_smem();
             }
             tc_fence_before_sync();
-            if (!bar_and(32 * kChainWarps, good)) { ok = false; break; }
-            tc_fence_after_sync();
-            if (kOut && tid == 0 && A.has_tm_out && seq0 + (int64_t)(cb + it + 1) * kChunk <= seq1) {
+            if (kOut) {
+                // MMA3 needs U only: the U warps meet on their own barrier and it
+                // is issued while the O warps finish the outputs (and one of them
+                // issues their TMA stores); everyone meets at the step's end.
+                if (q < 2) {
+                    good = bar_and_id(2, 32 * kChainWarps / 2, good);
+                } else {
+                    good = bar_and_id(3, 32 * kChainWarps / 2, good);
+                    if (tid == kOLeader && good && A.has_tm_out && seq0 + (int64_t)(cb + it + 1) * kChunk <= seq1) {
 #pragma unroll
-                for (int tl = 0; tl < kTcD / kTile; ++tl)
-                    tma_store_3d(&A.tm_out, st + L::kO0 + tl * TcRec::kTileBytes, tl * kTile, h,
-                                 (int)(seq0 + (int64_t)(cb + it) * kChunk));
-                bulk_commit();
+                        for (int tl = 0; tl < kTcD / kTile; ++tl)
+                            tma_store_3d(&A.tm_out, st + L::kO0 + tl * TcRec::kTileBytes, tl * kTile, h,
+                                         (int)(seq0 + (int64_t)(cb + it) * kChunk));
+                        bulk_commit();
+                    }
+                }
+            } else {
+                good = bar_and(32 * kChainWarps, good);
             }
-            if (tid == 0) {
+            tc_fence_after_sync();
+            if (tid == 0 && good) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_ss(tmem + NX, sdesc(smem_u32(st + L::kKE + ks * 2048), 8192, 1024, 2),
                                 sdesc(smem_u32(UO + ks * 2048), 8192, 1024, 2), id3, ks > 0);
                 mma_commit(mbar);
             }
-            good = mbar_wait(mbar, ph & 1, kWaitNs);
+            good = good && mbar_wait(mbar, ph & 1, kWaitNs);
             ++ph;
             tc_fence_after_sync();
             const float gam = ((const float*)(st + L::kGam))[i];
@@ -891,9 +903,9 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
             }
             write_X(1.f);
             fence_proxy_async_smem();
+            if (kOut && tid == kOLeader) bulk_wait_read_all();   // the stage's O tiles have been stored
             tc_fence_before_sync();
             ok = bar_and(32 * kChainWarps, good);
-            if (kOut && tid == 0) bulk_wait_read_all();        // the stage's O tiles have been stored
             if (ok && tid == 0) mbar_arrive(&empty[s]);
         }
         if (!ok) {

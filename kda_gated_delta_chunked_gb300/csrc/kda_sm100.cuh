@@ -67,6 +67,16 @@ __device__ __forceinline__ bool bar_and(uint32_t nthreads, bool v) {
     return r != 0;
 }
 
+// The same on named barrier `id` (2..15), for a subset of the block's warps.
+__device__ __forceinline__ bool bar_and_id(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n"
+        " bar.red.and.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r) : "r"((uint32_t)v), "r"(id), "r"(nthreads) : "memory");
+    return r != 0;
+}
+
 // -------------------------------------------------------------- async copies
 // Generic-proxy writes to shared memory -> visible to the async proxy (TMA
 // stores, tcgen05.mma operand reads).
