@@ -12,9 +12,9 @@
 //           dk_t = beta_t dS e - S' de;      dS' = dS - k_t de^T
 //   decay:  dlog_alpha_t = alpha_t o rowsum(dS' o S_{t-1});     dS <- Diag(alpha_t) dS'
 //
-// Columns of S (and of dS) never mix, so a CTA owns a tile of 16 or 32 state
-// columns of one (sequence, head) (16 when that is needed to give every SM a
-// CTA) and walks the whole sequence: first forward, keeping the
+// Columns of S (and of dS) never mix, so a CTA owns a tile of 8, 16 or 32
+// state columns of one (sequence, head) (the widest that still gives every SM
+// a CTA) and walks the whole sequence: first forward, keeping the
 // tile's state every kBlk tokens in the workspace, then backwards block by
 // block, recomputing the block's states into shared memory and applying the
 // rules above.  dv and the initial-state gradient belong to the tile; dq, dk,
@@ -35,7 +35,7 @@ constexpr int kBlk = 8;             // tokens between kept states
 // memory without bank conflicts); sums over the tile's columns combine the
 // warp's columns by shuffles and the 8 warps through red[].
 template <int D, int COLS> struct BwdSmem {
-    static constexpr int kRG = kBwdThreads / COLS;    // row groups (16 or 8: a power of two <= 32)
+    static constexpr int kRG = kBwdThreads / COLS;    // row groups (32, 16 or 8: a power of two <= 32)
     static constexpr int kRP = D / kRG;               // rows per thread
     float st[kBlk][kRP][COLS][kRG];                   // S_{t-1} of each token of the block, [.][a][j][rg]
     float k[kBlk][D], q[kBlk][D], alpha[kBlk][D];
@@ -263,8 +263,11 @@ kda_backward_reduce(const float* __restrict__ part, const DeviceHeader* __restri
 size_t backward_ckpt_bytes(int d, int H, int64_t chunks_ub) {
     return (size_t)chunks_ub * (kChunk / kBlk) * H * (size_t)d * d * sizeof(float);
 }
-// Columns per CTA: 16 when 32-column tiles would leave SMs idle.
-static int bwd_cols(int N, int H, int d) { return (int64_t)N * H * (d / 32) < 152 ? 16 : 32; }
+// Columns per CTA: fewer when wider tiles would leave SMs idle.
+static int bwd_cols(int N, int H, int d) {
+    const int64_t nh = (int64_t)N * H;
+    return nh * (d / 32) >= 152 ? 32 : nh * (d / 16) >= 152 ? 16 : 8;
+}
 
 size_t backward_part_bytes(int N, int d, int H, int64_t T) {
     return (size_t)(d / bwd_cols(N, H, d)) * T * H * (3 * (size_t)d + 1) * sizeof(float);
@@ -291,7 +294,9 @@ static cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t stream) {
 
 template <typename T, int D>
 static cudaError_t launch_bwd_cols(const BackwardArgs& a, cudaStream_t stream) {
-    return bwd_cols(a.N, a.H, D) == 16 ? launch_bwd<T, D, 16>(a, stream) : launch_bwd<T, D, 32>(a, stream);
+    const int cols = bwd_cols(a.N, a.H, D);
+    return cols == 8 ? launch_bwd<T, D, 8>(a, stream)
+                     : cols == 16 ? launch_bwd<T, D, 16>(a, stream) : launch_bwd<T, D, 32>(a, stream);
 }
 
 cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t stream) {

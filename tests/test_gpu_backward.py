@@ -92,3 +92,12 @@ def test_backward_deterministic(kda):
     torch.cuda.synchronize()
     for key in a:
         assert torch.equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("nseq,heads", [(10, 2), (20, 2), (4, 2)])
+def test_backward_tile_widths(kda, nseq, heads):
+    """Sequence x head counts that select 16-, 32- and 8-column tiles."""
+    lens = [(7 * i + 5) % 37 + 1 for i in range(nseq)]
+    d = prefill_inputs(custom(120 + nseq, lens, heads, 128, "bf16"))
+    do, dfin = _cotangents(d, 7, "bf16")
+    _compare(kda, d, do, dfin, f"{nseq} sequences x {heads} heads")
