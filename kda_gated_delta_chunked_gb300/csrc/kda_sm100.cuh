@@ -90,18 +90,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
-// 1-D bulk copy shared -> global (bulk async-group).
-__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 ::"l"(dst), "r"(smem_u32(src)), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the shared-memory sources of all committed bulk stores were read.
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// Wait until all committed bulk stores completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // 3-D tiled tensor load (TMA), completion counted on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
@@ -116,9 +109,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
                  ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z) : "memory");
-}
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -238,12 +228,6 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t k) {
     return r * 128u + ((((k >> 3) ^ (r & 7u)) & 7u) << 4) + (k & 7u) * 2u;
 }
 
-// Byte offset of element (k, n < 16) of an N = 16 MN-major bf16 operand without
-// swizzle: 8-row K groups of two 8 x 16-byte core matrices (256 bytes per group).
-// Descriptor: leading offset 256, stride offset 128; +512 bytes per 16 K rows.
-__host__ __device__ __forceinline__ uint32_t mn16_off(uint32_t k, uint32_t n) {
-    return (k >> 3) * 256u + (n >> 3) * 128u + (k & 7u) * 16u + (n & 7u) * 2u;
-}
 
 }  // namespace sm100
 }  // namespace kda
