@@ -14,10 +14,12 @@
 // is read once and written once: the step is bound by HBM bandwidth on the
 // 2 * d_k * d_v * 4 bytes of fp32 state per (sequence, head).
 //
-// Grid: (N*H, d_v / 32).  A CTA owns a d_k x 32 column tile of one state
-// (columns of S are independent).  256 threads: 4 threads cover the 32 columns
-// of a row with 32-byte vectors (the widest global access on sm_100+), 64 rows
-// per pass, d_k/64 passes held in registers between the reduction and the
+// Grid: (N*H, d_v / TILE).  A CTA owns a d_k x TILE column tile of one state
+// (columns of S are independent); TILE = 64 (97% of the measured copy
+// bandwidth on GB300, against 86% with 32-column tiles: fewer, longer CTAs and
+// fewer redundant q/k/alpha loads).  256 threads: TILE / 8 threads cover a row
+// with 32-byte vectors (the widest global access on sm_100+), 256 / (TILE / 8)
+// rows per pass, the passes held in registers between the reduction and the
 // update.  State loads are issued before the small q/k/alpha staging so their
 // latency overlaps it; loads and stores carry an evict-first L2 hint because
 // the state is touched exactly once per step.
@@ -26,7 +28,7 @@
 
 namespace kda {
 
-constexpr int kDecTile = 32;     // state columns per CTA
+constexpr int kDecTile = 64;     // state columns per CTA (at most D)
 constexpr int kDecThreads = 256;
 
 struct f8 { float v[8]; };
@@ -49,18 +51,19 @@ __device__ __forceinline__ void st_stream_f8(float* p, const f8& x) {
                     "r"(__float_as_uint(x.v[6])), "r"(__float_as_uint(x.v[7])) : "memory");
 }
 
-template <typename T, int D>
+template <typename T, int D, int TILE>
 __global__ void __launch_bounds__(kDecThreads)
 kda_decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                        const T* __restrict__ log_alpha, int la_scalar, const T* __restrict__ beta,
                        float* __restrict__ state, T* __restrict__ out, int H) {
-    constexpr int kRowsPerPass = kDecThreads / 4;   // 64
+    constexpr int kTPR = TILE / 8;                  // threads per row of the tile (8 floats each)
+    constexpr int kRowsPerPass = kDecThreads / kTPR;
     constexpr int kPasses = D / kRowsPerPass;       // rows per thread
     const int nh = blockIdx.x;                      // (sequence, head) pair, = n * H + h
-    const int col0 = blockIdx.y * kDecTile;
+    const int col0 = blockIdx.y * TILE;
     const int tid = threadIdx.x;
-    const int rsub = tid >> 2;                      // row within a pass
-    const int c8 = tid & 3;                         // which 8-float group of the tile
+    const int rsub = tid / kTPR;                    // row within a pass
+    const int c8 = tid % kTPR;                      // which 8-float group of the tile
 
     float* S = state + (size_t)nh * D * D;
     f8 s[kPasses];
@@ -69,8 +72,8 @@ kda_decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
         s[p] = ld_stream_f8(S + (size_t)(p * kRowsPerPass + rsub) * D + col0 + c8 * 8);
 
     __shared__ float sh_alpha[D], sh_k[D], sh_q[D];
-    __shared__ float sh_red[kDecThreads / 32][2][kDecTile];
-    __shared__ __align__(16) float sh_u[kDecTile];
+    __shared__ float sh_red[kDecThreads / 32][2][TILE];
+    __shared__ __align__(16) float sh_u[TILE];
     __shared__ float sh_kq;
 
     const size_t vec = (size_t)nh * D;              // q, k, log_alpha, v rows of this (n, h)
@@ -103,17 +106,17 @@ kda_decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
             pq[j] += qr * s[p].v[j];
         }
     }
-    // Reduce over the 8 row groups of a warp (lanes differing in bits 2..4).
+    // Reduce over the row groups of a warp (lanes kTPR, 2 kTPR, ... apart).
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
+        for (int o = kTPR; o < 32; o <<= 1) {
             pk[j] += __shfl_xor_sync(0xffffffffu, pk[j], o);
             pq[j] += __shfl_xor_sync(0xffffffffu, pq[j], o);
         }
     }
     const int warp = tid >> 5, lane = tid & 31;
-    if (lane < 4) {
+    if (lane < kTPR) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             sh_red[warp][0][lane * 8 + j] = pk[j];
@@ -121,7 +124,7 @@ kda_decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
         }
     }
     __syncthreads();
-    if (tid < kDecTile) {
+    if (tid < TILE) {
         float p = 0.f, r = 0.f;
 #pragma unroll
         for (int w = 0; w < kDecThreads / 32; ++w) { p += sh_red[w][0][tid]; r += sh_red[w][1][tid]; }
@@ -149,8 +152,9 @@ template <typename T, int D>
 static cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* la,
                                  int la_scalar, const void* beta, float* state, void* out, int N, int H,
                                  cudaStream_t stream) {
-    dim3 grid((unsigned)N * H, D / kDecTile);
-    kda_decode_step_kernel<T, D><<<grid, kDecThreads, 0, stream>>>(
+    constexpr int kTile = kDecTile < D ? kDecTile : D;
+    dim3 grid((unsigned)N * H, D / kTile);
+    kda_decode_step_kernel<T, D, kTile><<<grid, kDecThreads, 0, stream>>>(
         (const T*)q, (const T*)k, (const T*)v, (const T*)la, la_scalar, (const T*)beta, state, (T*)out, H);
     return cudaGetLastError();
 }
