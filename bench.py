@@ -635,7 +635,7 @@ def main():
                     help="one sequence of this many tokens with the workload's distributions (profiling case)")
     ap.add_argument("--decode-reps", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--e2e-pieces", type=int, default=8)
+    ap.add_argument("--e2e-pieces", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=2048)
     ap.add_argument("--no-decode", action="store_true")
