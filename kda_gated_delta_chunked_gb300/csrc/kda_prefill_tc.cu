@@ -20,7 +20,9 @@
 //
 // Kernel (a), one CTA per (chunk, head), 256 threads, two CTAs per SM:
 //   1. Each thread owns 4 token rows x 8 key channels of the chunk: 16-byte
-//      loads of k, q, log_alpha, a running sum of log alpha within its rows
+//      loads of k, q, log_alpha (issued first thing, ahead of the set-up; a
+//      single sequence needs no table lookup for the chunk's bounds), a
+//      running sum of log alpha within its rows
 //      and a prefix over the 16 row groups through shared memory.  It then
 //      writes every scaled operand as bf16 with 16-byte stores, all
 //      token-major (no transposes): K~m, Q~m, K^m around a mid-chunk
@@ -33,8 +35,9 @@
 //      folded into the columns, so the solution needs no later rescaling).
 //      The solve runs in 16-column blocks from the right: the coupling to the
 //      already solved blocks is one small MMA (M=128, N=16) from the bf16 Y^
-//      and A^ (stored row by row, read MN-major), the 16 x 16 diagonal block a
-//      short fp32 recursion.  (Forming the diagonal-block inverses first, so
+//      and A^ (stored row by row, read MN-major), issued as soon as the block
+//      it reads is stored; the 16 x 16 diagonal block is a right-looking fp32
+//      recursion (one FMA per dependent step).  (Forming the diagonal-block inverses first, so
 //      that the sequential part is only the MMAs, was measured 1% slower: the
 //      recursion's work moves, it does not shrink.)
 //   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~m | V] with K~m read MN-major
@@ -97,6 +100,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&p);
 }
+// 2^x with the special-function unit's instruction (relative error ~2^-22 in
+// the PTX ISA); used where x is known to lie well inside [-126, 127].
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// Read-only global loads kept in program order (volatile), so they are issued
+// where written even when a later branch could skip their use.
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_nc_u16(const void* p) {
+    unsigned short r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
 __device__ __forceinline__ float bf_lo(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
 
@@ -111,7 +133,7 @@ struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per 
                                                 // MMA-a A, then MMA-b B (MN-major) and Q~m for the epilogue
     static constexpr uint32_t kOpB1 = 49152;    // MMA-a B K^m, K-major, 2 K-blocks x 8 KB; then:
     static constexpr uint32_t kAt = 49152;      //   A^ by 16-column blocks, MN-major 32B-swizzle, 4 x 2 KB
-    static constexpr uint32_t kAt32 = 57344;    //   diagonal 16 x 16 blocks of A^ transposed, fp32, 4 KB
+    static constexpr uint32_t kAt32 = 57344;    //   diagonal 16 x 16 blocks of A^, fp32 [64 rows][16], 4 KB
     static constexpr uint32_t kY = 65536;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB
     static constexpr uint32_t kPart = 65536;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
     static constexpr uint32_t kGS = 49152;      // (slow path, before A^) g, fp32 [64][128], 32 KB
@@ -138,24 +160,32 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 // Column block J (16 columns) of the solve Y^ (I + A^) = RHS for row `tid`
 // (threads 0..127) of Y^: the right-hand side (from the Gram / Q~ K^T
 // accumulator still in TMEM columns 0..63), minus the coupling to the solved
-// blocks on the right (one MMA from the bf16 Y^ and A^ into TMEM columns
-// 64..79), then the in-block recursion on the fp32 diagonal block; stored to
-// Y^ as bf16.  Threads 128..255 only take part in the barrier.
+// blocks on the right, then the in-block recursion on the fp32 diagonal block;
+// stored to Y^ as bf16.  Threads 128..255 only take part in the barrier.
+//
+// The coupling of block J' to block ks > J' is one MMA (M=128, N=16, K=16) from
+// the bf16 Y^ and A^ into TMEM columns 64 + 16 J'.  They are issued as soon as
+// block ks is stored: at the start of block J, the products of block J+1 with
+// every block J' <= J, the one for J itself first and committed, so each block
+// waits for a single MMA; the others run during its recursion and are covered
+// by the next commit (one thread's MMAs complete in order).
 template <int J>
 __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const float* s_beta, uint64_t* bar,
                                           int* s_flag, uint32_t& mph, bool& abort) {
     const int tid = threadIdx.x, warp = tid >> 5;
     uint8_t* yop = sm + SmemA::kY;
     if (J < 3 && tid == 0 && !abort) {
-#pragma unroll
-        for (int ks = J + 1; ks < 4; ++ks)
-            mma_bf16_ss(tmem + 64, sdesc_k_sw128(smem_u32(yop + ks * 32)),
-                        sdesc(smem_u32(sm + SmemA::kAt + J * 2048 + ks * 512), 2048, 256, 6),
-                        idesc_bf16(128, 16, 0, 1), ks > J + 1);
+        const uint64_t ya = sdesc_k_sw128(smem_u32(yop + (J + 1) * 32));
+        const uint32_t id = idesc_bf16(128, 16, 0, 1);
+        mma_bf16_ss(tmem + 64 + 16 * J, ya, sdesc(smem_u32(sm + SmemA::kAt + J * 2048 + (J + 1) * 512), 2048, 256, 6),
+                    id, J + 1 < 3);
         mma_commit(bar);
+#pragma unroll
+        for (int jt = J - 1; jt >= 0; --jt)
+            mma_bf16_ss(tmem + 64 + 16 * jt, ya,
+                        sdesc(smem_u32(sm + SmemA::kAt + jt * 2048 + (J + 1) * 512), 2048, 256, 6), id, J + 1 < 3);
     }
     if (warp < 4) {
-        const float4* at32v = (const float4*)(sm + SmemA::kAt32);
         float z[16];
         if (warp < 2) {
 #pragma unroll
@@ -172,23 +202,25 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
             if (!abort && !mbar_wait(bar, mph & 1, kWaitNs)) s_flag[1] = 1;
             tc_fence_after_sync();
             float dd[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 64), dd);
+            tmem_ld16(tmem_addr(tmem, 32 * warp, 64 + 16 * J), dd);
             tmem_wait_ld();
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) z[jj] -= dd[jj];
         }
+        // Right-looking: once z[m] is final, remove its share A^[m][jj] from
+        // every z[jj], jj < m.  The dependent chain is one FMA per step.
+        const float4* arow = (const float4*)(sm + SmemA::kAt32) + 16 * J * 4;
 #pragma unroll
-        for (int jj = 14; jj >= 0; --jj) {
-            float acc = z[jj];
+        for (int m = 15; m >= 1; --m) {
+            const float zm = z[m];
 #pragma unroll
-            for (int g4 = (jj + 1) >> 2; g4 < 4; ++g4) {
-                const float4 a = at32v[(J * 16 + jj) * 4 + g4];
-                if (4 * g4 + 0 > jj) acc = fmaf(-z[4 * g4 + 0], a.x, acc);
-                if (4 * g4 + 1 > jj) acc = fmaf(-z[4 * g4 + 1], a.y, acc);
-                if (4 * g4 + 2 > jj) acc = fmaf(-z[4 * g4 + 2], a.z, acc);
-                if (4 * g4 + 3 > jj) acc = fmaf(-z[4 * g4 + 3], a.w, acc);
+            for (int g4 = 0; 4 * g4 < m; ++g4) {
+                const float4 a = arow[m * 4 + g4];
+                if (4 * g4 + 0 < m) z[4 * g4 + 0] = fmaf(-zm, a.x, z[4 * g4 + 0]);
+                if (4 * g4 + 1 < m) z[4 * g4 + 1] = fmaf(-zm, a.y, z[4 * g4 + 1]);
+                if (4 * g4 + 2 < m) z[4 * g4 + 2] = fmaf(-zm, a.z, z[4 * g4 + 2]);
+                if (4 * g4 + 3 < m) z[4 * g4 + 3] = fmaf(-zm, a.w, z[4 * g4 + 3]);
             }
-            z[jj] = acc;
         }
         uint32_t p[8];
 #pragma unroll
@@ -210,7 +242,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
                    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ log_alpha,
                    const __nv_bfloat16* __restrict__ beta, const int32_t* __restrict__ cu,
                    DeviceHeader* __restrict__ hdr, const int32_t* __restrict__ chunk_first, int N, int H,
-                   uint8_t* __restrict__ recs) {
+                   int64_t T, uint8_t* __restrict__ recs) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* s_beta = (float*)(sm + SmemA::kMisc);                 // [64]
@@ -223,16 +255,54 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, h = blockIdx.y;
-    // The status word, the chunk's sequence and its bounds are loaded together
-    // (one memory round trip for a single sequence); the tables are always
-    // written, so reading them before the status check is safe.
-    const int status = hdr->status, total_chunks = hdr->total_chunks;
-    const int n = N == 1 ? 0 : chunk_owner(chunk_first, N, c);
-    const int64_t seq_begin = cu[n], seq_end = cu[n + 1];
-    const int c_first = chunk_first[n];
-    if (status != KDA_OK || c >= total_chunks) return;
-    const int64_t t0 = seq_begin + (int64_t)(c - c_first) * kChunk;
-    const int len = (int)min64(kChunk, seq_end - t0);
+    int64_t t0;
+    int len, status;
+    if (N == 1) {
+        // One sequence starts at token 0 (a cu_seqlens that does not is flagged
+        // in the status word), so the chunk's bounds follow from c alone and
+        // the input loads below wait for no table.
+        status = hdr->status;
+        t0 = (int64_t)c * kChunk;
+        if (t0 >= T) return;
+        len = (int)min64(kChunk, T - t0);
+    } else {
+        // The status word, the chunk's sequence and its bounds are loaded
+        // together; the tables are always written, so reading them before the
+        // status check is safe.
+        status = hdr->status;
+        const int total_chunks = hdr->total_chunks;
+        const int n = chunk_owner(chunk_first, N, c);
+        const int64_t seq_begin = cu[n], seq_end = cu[n + 1];
+        const int c_first = chunk_first[n];
+        if (status != KDA_OK || c >= total_chunks) return;
+        t0 = seq_begin + (int64_t)(c - c_first) * kChunk;
+        len = (int)min64(kChunk, seq_end - t0);
+    }
+
+    // ---- pass A: thread owns rows 4R..4R+3, channels 8C..8C+7.  The 16-byte
+    // loads of k, q, log alpha (and beta) are issued first, before the status
+    // check and the set-up below, so their latency overlaps both (volatile:
+    // the compiler keeps them ahead of the status branch).
+    const int R = tid >> 4, C = tid & 15;
+    const size_t rs = (size_t)H * kTcD;                       // elements between tokens
+    const size_t base = ((size_t)t0 * H + h) * kTcD + 8 * C;
+    uint4 kr[4], qr[4], lr[4];
+    uint32_t lsr[4], braw = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 4 * R + i;
+        const size_t gi = base + (size_t)r * rs;
+        kr[i] = qr[i] = lr[i] = make_uint4(0u, 0u, 0u, 0u);
+        lsr[i] = 0;
+        if (r < len) {
+            kr[i] = ld_nc_v4(k + gi);
+            qr[i] = ld_nc_v4(q + gi);
+            if (kScalarGate) lsr[i] = ld_nc_u16(log_alpha + (size_t)(t0 + r) * H + h);   // one gate per (token, head)
+            else lr[i] = ld_nc_v4(log_alpha + gi);
+        }
+    }
+    if (tid < len) braw = ld_nc_u16(beta + (size_t)(t0 + tid) * H + h);
+    if (status != KDA_OK) return;
     uint8_t* rec = recs + ((size_t)c * H + h) * TcRec::kBytes;
 
     if (tid == 0) {
@@ -248,34 +318,23 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         tma_load_3d(sm + SmemA::kV, &tm_v, 0, h, (int)t0, &bars[0]);
         tma_load_3d(sm + SmemA::kV + 8192, &tm_v, 64, h, (int)t0, &bars[0]);
     }
-    if (tid < kChunk) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+    if (tid < kChunk) s_beta[tid] = __uint_as_float(braw << 16);
     if (warp == 0) { tmem_alloc(s_tmem, 256); tmem_relinquish(); }
 
-    // ---- pass A: thread owns rows 4R..4R+3, channels 8C..8C+7.  16-byte loads,
-    // running sum of log alpha (log2 units) within the 4 rows.
-    const int R = tid >> 4, C = tid & 15;
-    const size_t rs = (size_t)H * kTcD;                       // elements between tokens
-    const size_t base = ((size_t)t0 * H + h) * kTcD + 8 * C;
+    // Running sum of log alpha (log2 units) within the thread's 4 rows.
     float gl[4][8];
-    uint4 kr[4], qr[4];
     {
         float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int r = 4 * R + i;
-            const bool ok = r < len;
-            const size_t gi = base + (size_t)r * rs;
-            const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
             float la[8];
-            if (kScalarGate) {                  // one gate per (token, head), all channels
-                const float l = ok ? __bfloat162float(log_alpha[(size_t)(t0 + r) * H + h]) : 0.f;
+            if (kScalarGate) {
+                const float l = __uint_as_float(lsr[i] << 16);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) la[e] = l;
             } else {
-                unpack8(ok ? *(const uint4*)(log_alpha + gi) : z4, la);
+                unpack8(lr[i], la);
             }
-            kr[i] = ok ? *(const uint4*)(k + gi) : z4;
-            qr[i] = ok ? *(const uint4*)(q + gi) : z4;
 #pragma unroll
             for (int e = 0; e < 8; ++e) { s8[e] = fmaf(la[e], kLog2e, s8[e]); gl[i][e] = s8[e]; }
         }
@@ -340,6 +399,14 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         uint8_t* opB1 = sm + SmemA::kOpB1 + kb * 8192;
         uint8_t* ke = rec + TcRec::kKE + kb * 8192;
         float* gS = (float*)(sm + SmemA::kGS);
+        // On the fast path g_0 - g_C <= 100 and g_r, g_m lie in [g_C, g_0]
+        // (log alpha <= 0), so every exponent below is within [-100, 100].
+        float dm[8], fC[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            dm[e] = gbase[e] - gm[e];
+            fC[e] = slow ? 0.f : ex2_fast(gC[e] - gm[e]);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = 4 * R + i;
@@ -348,15 +415,16 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             unpack8(qr[i], qv);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float g = gbase[e] + gl[i][e];
                 if (!slow) {
-                    const float e1 = exp2f(g - gm[e]);        // 2^(g_r - g_m)
-                    const float e2 = exp2f(gm[e] - g);        // 2^(g_m - g_r)
+                    const float dr = gl[i][e] + dm[e];         // g_r - g_m
+                    const float e1 = ex2_fast(dr);             // 2^(g_r - g_m)
+                    const float e2 = ex2_fast(-dr);            // 2^(g_m - g_r)
                     km[e] = kv[e] * e1;
                     qm[e] = qv[e] * e1;
                     kh[e] = kv[e] * e2;
-                    kend[e] = kh[e] * exp2f(gC[e] - gm[e]);  // k 2^(g_C - g_r) <= |k|
+                    kend[e] = kh[e] * fC[e];                   // k 2^(g_C - g_r) <= |k|
                 } else {
+                    const float g = gbase[e] + gl[i][e];
                     const float e3 = exp2f(g);
                     km[e] = kv[e] * e3;
                     qm[e] = qv[e] * e3;
@@ -424,24 +492,25 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     abort = s_flag[1] != 0;
 
     // A^[i][j] = beta_j G[i][j] (j < i) row by row into the 16-column blocks
-    // (MN-major, rows m = i), and the diagonal blocks transposed into At32.
+    // (MN-major, rows m = i), and the diagonal blocks row by row into At32.
     {
         const int quarter = warp & 3, half = warp >> 2;
         if (quarter < 2) {
-            const int i = quarter * 32 + lane, ii = i & 15;
+            const int i = quarter * 32 + lane;
             float* at32 = (float*)(sm + SmemA::kAt32);
 #pragma unroll 1
             for (int j0 = 32 * half; j0 < 32 * half + 32; j0 += 16) {
                 float f[16];
                 tmem_ld16(tmem_addr(tmem, 32 * quarter, j0), f);
                 tmem_wait_ld();
-                const bool diag = (j0 >> 4) == (i >> 4);
                 float a[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = j0 + jj;
-                    a[jj] = (j < i) ? s_beta[j] * f[jj] : 0.f;
-                    if (diag) at32[j * 16 + ii] = a[jj];
+                for (int jj = 0; jj < 16; ++jj) a[jj] = (j0 + jj < i) ? s_beta[j0 + jj] * f[jj] : 0.f;
+                if ((j0 >> 4) == (i >> 4)) {           // diagonal block: row i, fp32
+                    float4* dst = (float4*)(at32 + i * 16);
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4)
+                        dst[e4] = make_float4(a[4 * e4], a[4 * e4 + 1], a[4 * e4 + 2], a[4 * e4 + 3]);
                 }
                 uint8_t* blk = sm + SmemA::kAt + (j0 >> 4) * 2048;
                 float lo[8], hi[8];
@@ -1046,7 +1115,7 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
         if (!make_v_map(&mv, a.v, T, a.H)) return cudaErrorInvalidValue;
         intra<<<dim3(a.chunks_ub, a.H), kAThreads, SmemA::kBytes, stream>>>(
             mv, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.la,
-            (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, (uint8_t*)a.recs);
+            (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, T, (uint8_t*)a.recs);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[1], stream)) != cudaSuccess) return e;
