@@ -45,7 +45,10 @@
 //      are rescaled per channel in the epilogue, Q' = Q~ - P T K~.
 //   5. The records kernel (b) reads are written as ready-to-copy shared-memory
 //      images: [W; Q'] (K-major, 128-byte swizzle), K^end (token-major), U0 /
-//      O0 in 16-column tiles, Gamma.
+//      O0 in 16-column tiles, Gamma.  [W; Q'] and U0 / O0 are staged in shared
+//      memory (in place over the dead operands) and copied out with coalesced
+//      16-byte stores: written straight from the accumulator rows, every lane
+//      of a store touched its own 128-byte line (9% slower).
 // Chunks whose cumulative decay spans more than 2^100 inside the chunk cannot
 // use the mid-reference factorisation in fp32; for those the Gram and Q~ K^T
 // rows are formed on CUDA cores with exp(g_i - g_j) (never > 1) inside the
@@ -561,7 +564,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         const int quarter = warp & 3, half = warp >> 2;
         const int i = (quarter & 1) * 32 + lane;      // token row within the chunk
         const bool top = quarter < 2;
-        uint8_t* a1 = rec + TcRec::kA1;
+        uint8_t* a1 = sm + SmemA::kOpA;               // [W; Q'] image, in place over [K~m; Q~m]
         const uint8_t* qm = sm + SmemA::kOpA;
 #pragma unroll 1
         for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
@@ -588,7 +591,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin)) = pack8(lo);
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = pack8(hi);
         }
-        uint8_t* uo = rec + (top ? TcRec::kU0 : TcRec::kO0);
+        uint8_t* uo = sm + SmemA::kAt + (top ? 0 : TcRec::kO0 - TcRec::kU0);   // U0 | O0 images
 #pragma unroll 1
         for (int t = 4 * half; t < 4 * half + 4; ++t) {
             float f[16];
@@ -607,6 +610,15 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
+    if (!abort) {                      // coalesced copy of the staged images to the record
+        static_assert(SmemA::kAt + 2 * (TcRec::kO0 - TcRec::kU0) <= SmemA::kMisc, "staging fits");
+#pragma unroll 4
+        for (int e = tid; e < 4096; e += kAThreads) {
+            const uint32_t off = e < 2048 ? (uint32_t)e * 16u : (uint32_t)(e - 2048) * 16u;
+            const uint4 x = *(const uint4*)(sm + (e < 2048 ? SmemA::kOpA : SmemA::kAt) + off);
+            *(uint4*)(rec + (e < 2048 ? TcRec::kA1 : TcRec::kU0) + off) = x;
+        }
+    }
     if (tid == 0) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
 }
 
