@@ -41,14 +41,12 @@
 //      that the sequential part is only the MMAs, was measured 1% slower: the
 //      recursion's work moves, it does not shrink.)
 //   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~m | V] with K~m read MN-major
+//      (the [K~m] half's K-steps issued as the solve stores each block of Y^)
 //      from the MMA-a operand; since K~ = K~m Diag(2^g_m), W, P T K~ and Q~
 //      are rescaled per channel in the epilogue, Q' = Q~ - P T K~.
 //   5. The records kernel (b) reads are written as ready-to-copy shared-memory
 //      images: [W; Q'] (K-major, 128-byte swizzle), K^end (token-major), U0 /
-//      O0 in 16-column tiles, Gamma.  [W; Q'] and U0 / O0 are staged in shared
-//      memory (in place over the dead operands) and copied out with coalesced
-//      16-byte stores: written straight from the accumulator rows, every lane
-//      of a store touched its own 128-byte line (9% slower).
+//      O0 in 16-column tiles, Gamma.
 // Chunks whose cumulative decay spans more than 2^100 inside the chunk cannot
 // use the mid-reference factorisation in fp32; for those the Gram and Q~ K^T
 // rows are formed on CUDA cores with exp(g_i - g_j) (never > 1) inside the
@@ -129,6 +127,11 @@ __device__ __forceinline__ float bf_hi(uint32_t p) { return __uint_as_float(p & 
 // Kernel (a)
 // ---------------------------------------------------------------------------
 constexpr int kAThreads = 256;
+// TMEM columns: MMA-b's two halves at 0..127 ([K~m]) and 128..255 ([V]); until
+// MMA-b's second half, the Gram / Q~ K^T block sits at 128..191 and the
+// coupling accumulators at 192..239.
+constexpr uint32_t kTmGram = 128;
+constexpr uint32_t kTmCpl = 192;
 
 struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per SM
     static constexpr uint32_t kV = 0;           // V tile (TMA, 128-byte swizzle), 2 x [64 tok x 64 ch]
@@ -180,13 +183,16 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
     if (J < 3 && tid == 0 && !abort) {
         const uint64_t ya = sdesc_k_sw128(smem_u32(yop + (J + 1) * 32));
         const uint32_t id = idesc_bf16(128, 16, 0, 1);
-        mma_bf16_ss(tmem + 64 + 16 * J, ya, sdesc(smem_u32(sm + SmemA::kAt + J * 2048 + (J + 1) * 512), 2048, 256, 6),
+        mma_bf16_ss(tmem + kTmCpl + 16 * J, ya, sdesc(smem_u32(sm + SmemA::kAt + J * 2048 + (J + 1) * 512), 2048, 256, 6),
                     id, J + 1 < 3);
         mma_commit(bar);
 #pragma unroll
         for (int jt = J - 1; jt >= 0; --jt)
-            mma_bf16_ss(tmem + 64 + 16 * jt, ya,
+            mma_bf16_ss(tmem + kTmCpl + 16 * jt, ya,
                         sdesc(smem_u32(sm + SmemA::kAt + jt * 2048 + (J + 1) * 512), 2048, 256, 6), id, J + 1 < 3);
+        // K-step J+1 of MMA-b's first half, Y^ [K~m], into columns 0..127.
+        mma_bf16_ss(tmem, ya, sdesc(smem_u32(sm + SmemA::kOpA + (J + 1) * 2048), 16384, 1024, 2),
+                    idesc_bf16(128, 128, 0, 1), J + 1 < 3);
     }
     if (warp < 4) {
         float z[16];
@@ -196,7 +202,7 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
         } else {
             const int i = tid - 64;
             float f[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * J), f);
+            tmem_ld16(tmem_addr(tmem, 32 * warp, kTmGram + 16 * J), f);
             tmem_wait_ld();
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) z[jj] = (16 * J + jj <= i) ? f[jj] * s_beta[16 * J + jj] : 0.f;
@@ -205,7 +211,7 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
             if (!abort && !mbar_wait(bar, mph & 1, kWaitNs)) s_flag[1] = 1;
             tc_fence_after_sync();
             float dd[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 64 + 16 * J), dd);
+            tmem_ld16(tmem_addr(tmem, 32 * warp, kTmCpl + 16 * J), dd);
             tmem_wait_ld();
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) z[jj] -= dd[jj];
@@ -305,7 +311,8 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         }
     }
     if (tid < len) braw = ld_nc_u16(beta + (size_t)(t0 + tid) * H + h);
-    if (status != KDA_OK) return;
+    // (a single sequence checks the status word after the prefix below, before
+    // its first write, so the set-up does not wait for it)
     uint8_t* rec = recs + ((size_t)c * H + h) * TcRec::kBytes;
 
     if (tid == 0) {
@@ -382,6 +389,11 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         gC[0] = e.x; gC[1] = e.y; gC[2] = e.z; gC[3] = e.w; gC[4] = f.x; gC[5] = f.y; gC[6] = f.z; gC[7] = f.w;
     }
     const uint32_t tmem = *s_tmem;
+    if (status != KDA_OK) {            // uniform; nothing has been written yet
+        if (warp == 0) tmem_dealloc(tmem, 256);
+        if (tid == 0) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
+        return;
+    }
     const bool slow = s_flag[0] != 0;
     if (slow) {
 #pragma unroll
@@ -453,7 +465,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kb = ks >> 2, kin = ks & 3;
-                mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kOpA + kb * 16384 + kin * 32)),
+                mma_bf16_ss(tmem + kTmGram, sdesc_k_sw128(smem_u32(sm + SmemA::kOpA + kb * 16384 + kin * 32)),
                             sdesc_k_sw128(smem_u32(sm + SmemA::kOpB1 + kb * 8192 + kin * 32)), id, ks > 0);
             }
             mma_commit(&bars[1]);
@@ -485,7 +497,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
                 }
                 f[jj] = acc;
             }
-            tmem_st16(tmem_addr(tmem, 32 * quarter, j0), f);
+            tmem_st16(tmem_addr(tmem, 32 * quarter, kTmGram + j0), f);
         }
         tmem_wait_st();
     }
@@ -504,7 +516,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 #pragma unroll 1
             for (int j0 = 32 * half; j0 < 32 * half + 32; j0 += 16) {
                 float f[16];
-                tmem_ld16(tmem_addr(tmem, 32 * quarter, j0), f);
+                tmem_ld16(tmem_addr(tmem, 32 * quarter, kTmGram + j0), f);
                 tmem_wait_ld();
                 float a[16];
 #pragma unroll
@@ -535,15 +547,15 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     inv_block<1>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
     inv_block<0>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
 
-    // ---- MMA-b: Y^ [K~m | V] -> [[W Em^-1, U0], [P T K~m, O0]].  Its issuing
-    // thread waits for the V tile first (the MMA reads it).
+    // ---- MMA-b: Y^ [K~m | V] -> [[W Em^-1, U0], [P T K~m, O0]].  K-steps 3..1
+    // of the [K~m] half were issued during the solve, as each block of Y^ was
+    // stored; here the last one and the [V] half, whose issuing thread waits
+    // for the V tile first (the MMA reads it).
     if (tid == 0 && !abort && !mbar_wait(&bars[0], 0, kWaitNs)) { s_flag[1] = 1; abort = true; }
     if (tid == 0 && !abort) {
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
-                        sdesc(smem_u32(sm + SmemA::kOpA + ks * 2048), 16384, 1024, 2), id, ks > 0);
+        mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kY)),
+                    sdesc(smem_u32(sm + SmemA::kOpA), 16384, 1024, 2), id, true);   // last K-step of the [K~m] half
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
             mma_bf16_ss(tmem + 128, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
