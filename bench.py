@@ -326,11 +326,15 @@ def run_ours(args, dist: Dist):
 
     # --- the same prefill with the scalar (Gated DeltaNet) gate
     if not args.no_scalar_gate:
-        res["scalar_gate"] = bench_scalar_gate(kda, args, stream, x, s0, out, sf, ws, w)
+        res["scalar_gate"] = bench_scalar_gate(kda, args, stream, x, s0, out, sf, ws, w, peaks, peak_src)
+
+    # --- the same prefill filling a prefix cache (state snapshots)
+    if not args.no_snapshots:
+        res["snapshots"] = bench_snapshots(kda, args, dev, stream, x, s0, out, sf, ws, w, peaks, peak_src, ms_step)
 
     # --- reverse mode of the prefill (training), on the 4,096-token workload
     if not args.no_backward:
-        res["backward"] = bench_backward(kda, args, dev, stream)
+        res["backward"] = bench_backward(kda, args, dev, stream, peaks, peak_src)
 
     # --- decode workload (state GB/s)
     if not args.no_decode:
@@ -347,39 +351,106 @@ def run_ours(args, dist: Dist):
     return res
 
 
-def bench_scalar_gate(kda, args, stream, x, s0, out, sf, ws, w):
+def timed_prefill(kda, desc, args_, stream, steps, warmup):
+    """Runs kda_prefill(desc, *args_) warmup + steps times; returns (ms per step,
+    mean intra-chunk kernel ms, mean chain ms) from CUDA events on `stream`
+    (the library records the phase events between its launches)."""
+    import ctypes
+
+    def run(phase=None):
+        if phase is not None:
+            arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in phase])
+            keep.append(arr)
+            desc.phase_events = ctypes.cast(arr, ctypes.c_void_p)
+        else:
+            desc.phase_events = None
+        rc = kda.kda_prefill(desc, *args_, stream) if len(args_) == 9 else \
+            kda.kda_prefill_snapshots(desc, *args_, stream)
+        if rc:
+            raise kda.KdaError("kda_prefill", rc)
+
+    keep = []
+    for _ in range(warmup):
+        run()
+    phases = [make_events(3) for _ in range(steps)]
+    t0, t1 = make_events(2)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        run(phases[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    desc.phase_events = None
+    if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
+        raise RuntimeError("device status not OK")
+    return (t0.elapsed_time(t1) / steps, statistics.mean(p[0].elapsed_time(p[1]) for p in phases),
+            statistics.mean(p[1].elapsed_time(p[2]) for p in phases))
+
+
+def hbm_roofline(kernel, nbytes, ms, peaks, peak_src):
+    a = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(a, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(a / peaks["hbm_gbs"], 4), "traffic": None, "kernel": kernel,
+            "peak_source": f"{peak_src} (copy)", "algorithmic_per_launch": nbytes, "launch_ms": round(ms, 4)}
+
+
+def bench_scalar_gate(kda, args, stream, x, s0, out, sf, ws, w, peaks, peak_src):
     """Prefill tokens/s of the same inputs with one gate per (token, head)
-    (channel 0 of log_alpha), the Gated DeltaNet form; secondary figure."""
+    (channel 0 of log_alpha), the Gated DeltaNet form; kernel (a) against HBM
+    on its algorithmic bytes (q, k, v per channel, one log alpha and one beta
+    per token and head)."""
     T, H, D = w.total_tokens, w.num_heads, w.d_k
     la = x["log_alpha"][:, :, 0].contiguous()
     desc = kda.make_desc(1, H, D, D, T, w.torch_dtype, ws, flags=kda.KDA_FLAG_SCALAR_GATE)
     steps = max(3, min(args.steps, 5))
-
-    def run():
-        rc = kda.kda_prefill(desc, x["q"], x["k"], x["v"], la, x["beta"], None, s0, out, sf, stream)
-        if rc:
-            raise kda.KdaError("kda_prefill", rc)
-
-    for _ in range(args.warmup):
-        run()
-    t0, t1 = make_events(2)
-    torch.cuda.synchronize()
-    t0.record(stream)
-    for _ in range(steps):
-        run()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
-        raise RuntimeError("device status not OK (scalar gate)")
-    ms = t0.elapsed_time(t1) / steps
+    ms, intra_ms, chain_ms = timed_prefill(kda, desc, (x["q"], x["k"], x["v"], la, x["beta"], None, s0, out, sf),
+                                           stream, steps, args.warmup)
     del la
+    esz = 2 if w.dtype == "bf16" else 4
+    per_tok = (3 * D + 2) * esz                     # q, k, v rows; one log alpha and one beta
     return {"workload": f"{w.name}, log_alpha one per (token, head)", "value": round(T / (ms * 1e-3), 1),
             "unit": "tokens/s", "ms_per_step": round(ms, 4), "steps": steps,
+            "intra_ms": round(intra_ms, 4), "chain_ms": round(chain_ms, 4),
+            "roofline": hbm_roofline("kda intra-chunk (a), scalar gate", T * H * per_tok, intra_ms, peaks, peak_src),
             "gpu_launches": prefill_launches(1, H, T) * steps}
 
 
-def bench_backward(kda, args, dev, stream):
-    """Prefill reverse mode (CUDA cores, fp32) on workload 1: tokens/s."""
+def bench_snapshots(kda, args, dev, stream, x, s0, out, sf, ws, w, peaks, peak_src, plain_ms, every=4096):
+    """The same prefill saving the state after every `every` tokens (a prefix
+    cache filled during the prefill): step time against the plain prefill and
+    kernel (a) against HBM as in the main line."""
+    T, H, D = w.total_tokens, w.num_heads, w.d_k
+    at = torch.tensor([[0, p] for p in range(every, T + 1, every)], dtype=torch.int32, device=dev)
+    m = at.shape[0]
+    snaps = torch.empty((m, H, D, D), dtype=torch.float32, device=dev)
+    desc = kda.make_desc(1, H, D, D, T, w.torch_dtype, ws)
+    steps = max(3, min(args.steps, 5))
+    ms, intra_ms, chain_ms = timed_prefill(
+        kda, desc, (x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, s0, out, sf, m, at, snaps),
+        stream, steps, args.warmup)
+    in_b = prefill_units(64, D, 2 if w.dtype == "bf16" else 4)[2]
+    res = {"workload": f"{w.name}, state saved every {every} tokens ({m} snapshots, "
+                       f"{m * H * D * D * 4 / 1e9:.2f} GB)",
+           "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+           "overhead_vs_plain": round(ms / plain_ms - 1.0, 4), "steps": steps,
+           "intra_ms": round(intra_ms, 4), "chain_ms": round(chain_ms, 4),
+           "roofline": hbm_roofline("kda intra-chunk (a)", T * H * in_b, intra_ms, peaks, peak_src),
+           "gpu_launches": (prefill_launches(1, H, T) + 1) * steps}
+    del snaps, at
+    return res
+
+
+def fp32_alu_peak(peaks):
+    """fp32 FMA peak of the CUDA cores: SMs x 128 fp32 lanes x 2 FLOP x max SM clock."""
+    p = torch.cuda.get_device_properties(torch.cuda.current_device())
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    return p.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def bench_backward(kda, args, dev, stream, peaks, peak_src):
+    """Prefill reverse mode (CUDA cores, fp32) on workload 1: tokens/s, and the
+    CUDA-core roofline on 20 d^2 FLOP per token and head (one forward step,
+    5 d^2, and its reverse, 15 d^2; the recomputation is not counted)."""
     w = workload(1)
     T, H, D = w.total_tokens, w.num_heads, w.d_k
     x = prefill_inputs(w, device=dev)
@@ -412,10 +483,17 @@ def bench_backward(kda, args, dev, stream):
     if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
         raise RuntimeError("device status not OK (backward)")
     ms = t0.elapsed_time(t1) / steps
+    flop = 20 * D * D * T * H
+    peak = fp32_alu_peak(peaks)
+    ach = flop / (ms * 1e-3) / 1e12
     return {"workload": w.name, "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(ms, 3), "steps": steps, "gpu_launches": 3 * steps,
-            "note": "fp32 CUDA cores, one CTA per (sequence, head, 32 state columns); gradients of q, k, v, "
-                    "log_alpha, beta and the initial state"}
+            "roofline": {"bound": "alu", "achieved": round(ach, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
+                         "frac": round(ach / peak, 4), "traffic": None, "kernel": "kda backward (CUDA cores)",
+                         "peak_source": f"SMs x 128 fp32 lanes x 2 x {peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
+                         "algorithmic_per_launch": flop, "launch_ms": round(ms, 4)},
+            "note": "fp32 CUDA cores, one CTA per (sequence, head, 8/16/32 state columns: the widest tile "
+                    "that still fills the SMs); gradients of q, k, v, log_alpha, beta and the initial state"}
 
 
 def bench_decode(kda, args, dev, stream, peaks, peak_src):
@@ -530,7 +608,8 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
             hho.copy_(dho, non_blocking=True)
         stream.wait_stream(d2h_s)
 
-    step()
+    for _ in range(2):                     # warm-up: first DMA over freshly pinned pages
+        step()
     torch.cuda.synchronize()
     steps = max(1, args.e2e_steps)
     t0, t1 = make_events(2)
@@ -643,6 +722,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scalar-gate", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-snapshots", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
