@@ -22,8 +22,8 @@
 //   1. Each thread owns 4 token rows x 8 key channels of the chunk: 16-byte
 //      loads of k, q, log_alpha (issued first thing, ahead of the set-up; a
 //      single sequence needs no table lookup for the chunk's bounds), a
-//      running sum of log alpha within its rows
-//      and a prefix over the 16 row groups through shared memory.  It then
+//      running sum of log alpha within its rows and a prefix over the 16 row
+//      groups through shared memory.  It then
 //      writes every scaled operand as bf16 with 16-byte stores, all
 //      token-major (no transposes): K~m, Q~m, K^m around a mid-chunk
 //      reference g_m, and K^end straight into the record.  V goes from HBM to
@@ -37,16 +37,19 @@
 //      already solved blocks is one small MMA (M=128, N=16) from the bf16 Y^
 //      and A^ (stored row by row, read MN-major), issued as soon as the block
 //      it reads is stored; the 16 x 16 diagonal block is a right-looking fp32
-//      recursion (one FMA per dependent step).  (Forming the diagonal-block inverses first, so
-//      that the sequential part is only the MMAs, was measured 1% slower: the
-//      recursion's work moves, it does not shrink.)
+//      recursion (one FMA per dependent step).  (Forming the diagonal-block
+//      inverses first, so that the sequential part is only the MMAs, was
+//      measured 1% slower: the recursion's work moves, it does not shrink.)
 //   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~m | V] with K~m read MN-major
 //      (the [K~m] half's K-steps issued as the solve stores each block of Y^)
 //      from the MMA-a operand; since K~ = K~m Diag(2^g_m), W, P T K~ and Q~
 //      are rescaled per channel in the epilogue, Q' = Q~ - P T K~.
 //   5. The records kernel (b) reads are written as ready-to-copy shared-memory
 //      images: [W; Q'] (K-major, 128-byte swizzle), K^end (token-major), U0 /
-//      O0 in 16-column tiles, Gamma.
+//      O0 in 16-column tiles, Gamma.  [W; Q'] and U0 / O0 are staged in shared
+//      memory (in place over the dead operands) and copied out with coalesced
+//      16-byte stores: written straight from the accumulator rows, every lane
+//      of a store touched its own 128-byte line (9% slower).
 // Chunks whose cumulative decay spans more than 2^100 inside the chunk cannot
 // use the mid-reference factorisation in fp32; for those the Gram and Q~ K^T
 // rows are formed on CUDA cores with exp(g_i - g_j) (never > 1) inside the
