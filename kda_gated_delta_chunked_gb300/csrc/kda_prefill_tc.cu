@@ -146,7 +146,8 @@ struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per 
     static constexpr uint32_t kY = 65536;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB
     static constexpr uint32_t kPart = 65536;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
     static constexpr uint32_t kGS = 49152;      // (slow path, before A^) g, fp32 [64][128], 32 KB
-    static constexpr uint32_t kMisc = 81920;    // beta[64], Em[128], barriers, TMEM slot, flags, g_C, g_0
+    static constexpr uint32_t kMisc = 81920;    // beta[64], Em[128], barriers, TMEM slot, flags, g_C, g_0,
+                                                // scalar gates[64]
     static constexpr uint32_t kBytes = kMisc + 2048 + 1024;
 };
 
@@ -264,6 +265,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     int* s_flag = (int*)(sm + SmemA::kMisc + 816);                // [0] slow path, [1] abort
     float* s_gtot = (float*)(sm + SmemA::kMisc + 1024);           // [128] g_C per channel
     float* s_g0 = (float*)(sm + SmemA::kMisc + 1536);             // [128] g of the first token
+    float* s_lg = (float*)(sm + SmemA::kMisc + 2048);             // [64] scalar gates of the chunk
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, h = blockIdx.y;
@@ -299,21 +301,24 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     const size_t rs = (size_t)H * kTcD;                       // elements between tokens
     const size_t base = ((size_t)t0 * H + h) * kTcD + 8 * C;
     uint4 kr[4], qr[4], lr[4];
-    uint32_t lsr[4], braw = 0;
+    uint32_t braw = 0, lraw = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int r = 4 * R + i;
         const size_t gi = base + (size_t)r * rs;
         kr[i] = qr[i] = lr[i] = make_uint4(0u, 0u, 0u, 0u);
-        lsr[i] = 0;
         if (r < len) {
             kr[i] = ld_nc_v4(k + gi);
             qr[i] = ld_nc_v4(q + gi);
-            if (kScalarGate) lsr[i] = ld_nc_u16(log_alpha + (size_t)(t0 + r) * H + h);   // one gate per (token, head)
-            else lr[i] = ld_nc_v4(log_alpha + gi);
+            if (!kScalarGate) lr[i] = ld_nc_v4(log_alpha + gi);
         }
     }
-    if (tid < len) braw = ld_nc_u16(beta + (size_t)(t0 + tid) * H + h);
+    // beta, and with the scalar gate the chunk's 64 gates, one per thread
+    // (loaded once and shared: 4 scalar loads per thread were 10% slower).
+    if (tid < len) {
+        braw = ld_nc_u16(beta + (size_t)(t0 + tid) * H + h);
+        if (kScalarGate) lraw = ld_nc_u16(log_alpha + (size_t)(t0 + tid) * H + h);
+    }
     // (a single sequence checks the status word after the prefix below, before
     // its first write, so the set-up does not wait for it)
     uint8_t* rec = recs + ((size_t)c * H + h) * TcRec::kBytes;
@@ -325,6 +330,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         s_flag[0] = 0;
         s_flag[1] = 0;
     }
+    if (kScalarGate && tid < kChunk) s_lg[tid] = __uint_as_float(lraw << 16);
     __syncthreads();
     if (tid == 0) {
         mbar_arrive_expect_tx(&bars[0], 16384);
@@ -342,7 +348,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         for (int i = 0; i < 4; ++i) {
             float la[8];
             if (kScalarGate) {
-                const float l = __uint_as_float(lsr[i] << 16);
+                const float l = s_lg[4 * R + i];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) la[e] = l;
             } else {
