@@ -179,6 +179,13 @@ def prefill_units(C=64, d=128, esz=2):
     return intra_flops, chain_flops, in_bytes, out_bytes
 
 
+def dense_issued_flops(C=64, d=128):
+    """Contraction FLOPs per token and head as the dense products are issued:
+    the C x C blocks A and P in full (2 C d each), T K~, T V and P U in full
+    (2 C d each), and the three d x d products of the chain (6 d^2)."""
+    return 2 * C * d * 2 + 2 * C * d * 3 + 6 * d * d
+
+
 def bench_workload(args):
     """The prefill workload of the step; ``--tokens T`` keeps its distributions
     and heads but makes it one sequence of T tokens (a smaller profiling case)."""
@@ -316,6 +323,10 @@ def run_ours(args, dist: Dist):
                    "l2": "inputs (%.1f GB per step) larger than L2; no flush" % (units * (in_b + out_b) / 1e9),
                    "parallelism": f"replicas x{dist.world} (independent problems)"},
         "pct_bf16_tc_peak": round(units * (intra_f + chain_f) / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+        # secondary: the dense products as issued, masked halves included (180,224 FLOP per
+        # token and head at C = 64, d = 128)
+        "pct_bf16_tc_peak_dense_as_issued": round(units * dense_issued_flops(64, D) / (ms_step * 1e-3) / 1e12
+                                                  / peaks["bf16_tflops"], 4),
         "pct_hbm_roofline": round(units * (in_b + out_b) / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
         "roofline": roofline,
         "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items() if kk != "files"}
