@@ -55,6 +55,17 @@ def test_scalar_gate_equals_broadcast_channel_gate(kda):
     assert torch.equal(out1, out2) and torch.equal(sf1, sf2)
 
 
+def test_scalar_gate_strong_decay(kda):
+    """Scalar gates strong enough (log alpha ~ -U(0.5, 5)) that full chunks take
+    the tensor-core kernel's CUDA-core Gram path, while the short tail chunks
+    (8 and 2 tokens) stay on the fast path."""
+    d = prefill_inputs(custom(75, [200, 64, 130], 2, 128, "bf16", la_lo=0.5, la_hi=5.0, gate="scalar"))
+    out, sf = _prefill(kda, d)
+    ro, rs = _oracle(d)
+    assert np.isfinite(host(out)).all() and np.isfinite(host(sf)).all()
+    assert_parity("scalar gate, strong decay", host(out), ro, host(sf), rs, "bf16")
+
+
 def test_scalar_gate_segment_scan(kda):
     """A long sequence (split into segments) with the scalar gate."""
     d = prefill_inputs(custom(73, [16384 + 100], 2, 128, "bf16", la_lo=0.0001, la_hi=0.05, gate="scalar"))
