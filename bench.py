@@ -622,6 +622,19 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
     for _ in range(2):                     # warm-up: first DMA over freshly pinned pages
         step()
     torch.cuda.synchronize()
+    # The host link's own rate right now (1 GiB of q's own bytes copied each
+    # way, values unchanged), so a run on a box whose host side is busy can be
+    # told from a slow pipeline.
+    probe = hx["q"].view(-1)[: min(hx["q"].numel(), 1 << 29)]
+    dprobe = dx["q"].view(-1)[: probe.numel()]
+    link = {}
+    for name, (dst_t, src_t) in (("h2d_gbs", (dprobe, probe)), ("d2h_gbs", (probe, dprobe))):
+        a, b = make_events(2)
+        a.record(stream)
+        dst_t.copy_(src_t, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        link[name] = round(probe.numel() * probe.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
     steps = max(1, args.e2e_steps)
     t0, t1 = make_events(2)
     torch.cuda.synchronize()
@@ -635,7 +648,7 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
     ms = t0.elapsed_time(t1) / steps
     return {"value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall * 1e3, 3),
-            "steps": steps, "host_buffers": "pinned",
+            "steps": steps, "host_buffers": "pinned", "link_probe": link,
             "pieces": pieces, "schedule": "H2D, prefill continuation and D2H of consecutive pieces overlap "
                                           "on three streams"}
 
@@ -724,7 +737,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="one sequence of this many tokens with the workload's distributions (profiling case)")
     ap.add_argument("--decode-reps", type=int, default=3)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-pieces", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=2048)
