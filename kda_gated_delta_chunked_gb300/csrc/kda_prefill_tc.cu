@@ -23,12 +23,12 @@
 //      loads of k, q, log_alpha (issued first thing, ahead of the set-up; a
 //      single sequence needs no table lookup for the chunk's bounds), a
 //      running sum of log alpha within its rows and a prefix over the 16 row
-//      groups through shared memory.  It then
-//      writes every scaled operand as bf16 with 16-byte stores, all
-//      token-major (no transposes): K~m, Q~m, K^m around a mid-chunk
-//      reference g_m, and K^end straight into the record.  V goes from HBM to
-//      the tensor core untouched (TMA, 128-byte swizzle).
-//   2. MMA-a (M=128, N=64, K=128): [K~m; Q~m] K^m^T gives the Gram block (rows
+//      groups through shared memory.  It then writes every scaled operand as
+//      bf16 with 16-byte stores, all token-major (no transposes): K~ = K 2^g,
+//      Q~ = Q 2^g, K^ = K 2^-g (g counted from the chunk start, in log2
+//      units), and K^end straight into the record.  V goes from HBM to the
+//      tensor core untouched (TMA, 128-byte swizzle).
+//   2. MMA-a (M=128, N=64, K=128): [K~; Q~] K^^T gives the Gram block (rows
 //      0..63) and Q~ K^T (rows 64..127) in one TMEM accumulator.
 //   3. With A^[i][j] = beta_j (K~ K^T)[i][j] (j < i), the rows of
 //      Y^ = [T; P T] solve  Y^ (I + A^) = [Diag(beta); P Diag(beta)]  (beta
@@ -40,21 +40,22 @@
 //      recursion (one FMA per dependent step).  (Forming the diagonal-block
 //      inverses first, so that the sequential part is only the MMAs, was
 //      measured 1% slower: the recursion's work moves, it does not shrink.)
-//   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~m | V] with K~m read MN-major
-//      (the [K~m] half's K-steps issued as the solve stores each block of Y^)
-//      from the MMA-a operand; since K~ = K~m Diag(2^g_m), W, P T K~ and Q~
-//      are rescaled per channel in the epilogue, Q' = Q~ - P T K~.
+//   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~ | V] with K~ read MN-major
+//      from the MMA-a operand (the [K~] half's K-steps issued as the solve
+//      stores each block of Y^); the epilogue forms Q' = Q~ - P T K~.  (A
+//      reference point in mid-chunk, so that K~ and K^ stay within 2^+-50,
+//      needed a per-channel rescaling in the epilogue and was 5% slower.)
 //   5. The records kernel (b) reads are written as ready-to-copy shared-memory
 //      images: [W; Q'] (K-major, 128-byte swizzle), K^end (token-major), U0 /
 //      O0 in 16-column tiles, Gamma.  [W; Q'] and U0 / O0 are staged in shared
 //      memory (in place over the dead operands) and copied out with coalesced
 //      16-byte stores: written straight from the accumulator rows, every lane
 //      of a store touched its own 128-byte line (9% slower).
-// Chunks whose cumulative decay spans more than 2^100 inside the chunk cannot
-// use the mid-reference factorisation in fp32; for those the Gram and Q~ K^T
-// rows are formed on CUDA cores with exp(g_i - g_j) (never > 1) inside the
-// channel sums and stored to TMEM where MMA-a would have put them, and the
-// reference point moves to the chunk start (g_m = 0).
+// Chunks whose cumulative decay from the chunk start exceeds 2^100 in some
+// channel cannot use this factorisation (K^ would leave the range where the
+// products stay finite in fp32); for those the Gram and Q~ K^T rows are formed
+// on CUDA cores with exp(g_i - g_j) (never > 1) inside the channel sums and
+// stored to TMEM where MMA-a would have put them.
 //
 // Kernel (b), one CTA per (sequence, head, segment of chunks), 16 consumer
 // warps and a producer warp: the producer streams each chunk's record into a
@@ -85,7 +86,7 @@ constexpr int kTcD = 128;                // head size handled here
 constexpr int kTile = 16;                // columns per tile of the U0 / O0 record images
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMaxSpanLog2 = 100.f;    // fast path if max_c (g_0 - g_C) <= 100 (log2 units)
+constexpr float kMaxSpanLog2 = 100.f;    // fast path if max_c (-g_C) <= 100 (log2 units, from the chunk start)
 
 // Record of one (chunk, head), bytes.
 struct TcRec {
@@ -130,7 +131,7 @@ __device__ __forceinline__ float bf_hi(uint32_t p) { return __uint_as_float(p & 
 // Kernel (a)
 // ---------------------------------------------------------------------------
 constexpr int kAThreads = 256;
-// TMEM columns: MMA-b's two halves at 0..127 ([K~m]) and 128..255 ([V]); until
+// TMEM columns: MMA-b's two halves at 0..127 ([K~]) and 128..255 ([V]); until
 // MMA-b's second half, the Gram / Q~ K^T block sits at 128..191 and the
 // coupling accumulators at 192..239.
 constexpr uint32_t kTmGram = 128;
@@ -138,16 +139,15 @@ constexpr uint32_t kTmCpl = 192;
 
 struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per SM
     static constexpr uint32_t kV = 0;           // V tile (TMA, 128-byte swizzle), 2 x [64 tok x 64 ch]
-    static constexpr uint32_t kOpA = 16384;     // [K~m; Q~m], K-major 128B-swizzle, 2 K-blocks x 16 KB;
-                                                // MMA-a A, then MMA-b B (MN-major) and Q~m for the epilogue
-    static constexpr uint32_t kOpB1 = 49152;    // MMA-a B K^m, K-major, 2 K-blocks x 8 KB; then:
+    static constexpr uint32_t kOpA = 16384;     // [K~; Q~], K-major 128B-swizzle, 2 K-blocks x 16 KB;
+                                                // MMA-a A, then MMA-b B (MN-major) and Q~ for the epilogue
+    static constexpr uint32_t kOpB1 = 49152;    // MMA-a B K^, K-major, 2 K-blocks x 8 KB; then:
     static constexpr uint32_t kAt = 49152;      //   A^ by 16-column blocks, MN-major 32B-swizzle, 4 x 2 KB
     static constexpr uint32_t kAt32 = 57344;    //   diagonal 16 x 16 blocks of A^, fp32 [64 rows][16], 4 KB
     static constexpr uint32_t kY = 65536;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB
     static constexpr uint32_t kPart = 65536;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
     static constexpr uint32_t kGS = 49152;      // (slow path, before A^) g, fp32 [64][128], 32 KB
-    static constexpr uint32_t kMisc = 81920;    // beta[64], Em[128], barriers, TMEM slot, flags, g_C, g_0,
-                                                // scalar gates[64]
+    static constexpr uint32_t kMisc = 81920;    // beta[64], barriers, TMEM slot, flags, g_C, scalar gates[64]
     static constexpr uint32_t kBytes = kMisc + 2048 + 1024;
 };
 
@@ -194,7 +194,7 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
         for (int jt = J - 1; jt >= 0; --jt)
             mma_bf16_ss(tmem + kTmCpl + 16 * jt, ya,
                         sdesc(smem_u32(sm + SmemA::kAt + jt * 2048 + (J + 1) * 512), 2048, 256, 6), id, J + 1 < 3);
-        // K-step J+1 of MMA-b's first half, Y^ [K~m], into columns 0..127.
+        // K-step J+1 of MMA-b's first half, Y^ [K~], into columns 0..127.
         mma_bf16_ss(tmem, ya, sdesc(smem_u32(sm + SmemA::kOpA + (J + 1) * 2048), 16384, 1024, 2),
                     idesc_bf16(128, 128, 0, 1), J + 1 < 3);
     }
@@ -259,12 +259,10 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* s_beta = (float*)(sm + SmemA::kMisc);                 // [64]
-    float* s_em = (float*)(sm + SmemA::kMisc + 256);             // [128] 2^(g_m) per channel
     uint64_t* bars = (uint64_t*)(sm + SmemA::kMisc + 768);       // [0] V tile, [1] MMAs
     uint32_t* s_tmem = (uint32_t*)(sm + SmemA::kMisc + 800);
     int* s_flag = (int*)(sm + SmemA::kMisc + 816);                // [0] slow path, [1] abort
     float* s_gtot = (float*)(sm + SmemA::kMisc + 1024);           // [128] g_C per channel
-    float* s_g0 = (float*)(sm + SmemA::kMisc + 1536);             // [128] g of the first token
     float* s_lg = (float*)(sm + SmemA::kMisc + 2048);             // [64] scalar gates of the chunk
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -360,16 +358,11 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         float4* part = (float4*)(sm + SmemA::kPart) + (R * kTcD + 8 * C) / 4;
         part[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
         part[1] = make_float4(s8[4], s8[5], s8[6], s8[7]);
-        if (R == 0) {                                   // g of the chunk's first token
-            float4* g0 = (float4*)(s_g0 + 8 * C);
-            g0[0] = make_float4(gl[0][0], gl[0][1], gl[0][2], gl[0][3]);
-            g0[1] = make_float4(gl[0][4], gl[0][5], gl[0][6], gl[0][7]);
-        }
     }
     __syncthreads();
     // Exclusive prefix over the 16 row groups, one thread per channel, in place;
-    // the chunk total g_C goes to s_gtot.  A chunk whose decay spans more than
-    // 2^kMaxSpanLog2 in some channel takes the slow path.
+    // the chunk total g_C goes to s_gtot.  A chunk whose decay from its start
+    // exceeds 2^kMaxSpanLog2 in some channel takes the slow path.
     if (tid < kTcD) {
         float* pc = (float*)(sm + SmemA::kPart) + tid;
         float x[16];
@@ -379,22 +372,20 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 #pragma unroll
         for (int rg = 0; rg < 16; ++rg) { pc[rg * kTcD] = acc; acc += x[rg]; }
         s_gtot[tid] = acc;
-        if (s_g0[tid] - acc > kMaxSpanLog2) s_flag[0] = 1;   // any writer sets 1
+        if (-acc > kMaxSpanLog2) s_flag[0] = 1;              // any writer sets 1
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    // g before this thread's rows, at row 31 (g_m) and at row 63 (g_C), for its 8 channels.
-    float gbase[8], gm[8], gC[8];
+    // g before this thread's rows and at row 63 (g_C), for its 8 channels.
+    float gbase[8], gC[8];
     {
         const float4* part = (const float4*)(sm + SmemA::kPart);
         const float4* tot = (const float4*)s_gtot;
         const float4 a = part[(R * kTcD + 8 * C) / 4], b = part[(R * kTcD + 8 * C) / 4 + 1];
-        const float4 c = part[(8 * kTcD + 8 * C) / 4], d = part[(8 * kTcD + 8 * C) / 4 + 1];
         const float4 e = tot[2 * C], f = tot[2 * C + 1];
         gbase[0] = a.x; gbase[1] = a.y; gbase[2] = a.z; gbase[3] = a.w;
         gbase[4] = b.x; gbase[5] = b.y; gbase[6] = b.z; gbase[7] = b.w;
-        gm[0] = c.x; gm[1] = c.y; gm[2] = c.z; gm[3] = c.w; gm[4] = d.x; gm[5] = d.y; gm[6] = d.z; gm[7] = d.w;
         gC[0] = e.x; gC[1] = e.y; gC[2] = e.z; gC[3] = e.w; gC[4] = f.x; gC[5] = f.y; gC[6] = f.z; gC[7] = f.w;
     }
     const uint32_t tmem = *s_tmem;
@@ -404,16 +395,9 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         return;
     }
     const bool slow = s_flag[0] != 0;
-    if (slow) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) gm[e] = 0.f;      // reference at the chunk start: nothing exceeds 1
-    }
     if (R == 0) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            s_em[8 * C + e] = exp2f(gm[e]);
-            ((float*)(rec + TcRec::kGam))[8 * C + e] = exp2f(gC[e]);
-        }
+        for (int e = 0; e < 8; ++e) ((float*)(rec + TcRec::kGam))[8 * C + e] = exp2f(gC[e]);
     }
 
     // ---- pass B: scaled operands for the thread's 4 rows x 8 channels.
@@ -423,14 +407,11 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         uint8_t* opB1 = sm + SmemA::kOpB1 + kb * 8192;
         uint8_t* ke = rec + TcRec::kKE + kb * 8192;
         float* gS = (float*)(sm + SmemA::kGS);
-        // On the fast path g_0 - g_C <= 100 and g_r, g_m lie in [g_C, g_0]
-        // (log alpha <= 0), so every exponent below is within [-100, 100].
-        float dm[8], fC[8];
+        // On the fast path -g_C <= 100 and g_r lies in [g_C, 0] (log alpha <= 0),
+        // so every exponent below is within [-100, 100].
+        float fC[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            dm[e] = gbase[e] - gm[e];
-            fC[e] = slow ? 0.f : ex2_fast(gC[e] - gm[e]);
-        }
+        for (int e = 0; e < 8; ++e) fC[e] = slow ? 0.f : ex2_fast(gC[e]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = 4 * R + i;
@@ -440,9 +421,9 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 if (!slow) {
-                    const float dr = gl[i][e] + dm[e];         // g_r - g_m
-                    const float e1 = ex2_fast(dr);             // 2^(g_r - g_m)
-                    const float e2 = ex2_fast(-dr);            // 2^(g_m - g_r)
+                    const float dr = gl[i][e] + gbase[e];      // g_r
+                    const float e1 = ex2_fast(dr);             // 2^g_r
+                    const float e2 = ex2_fast(-dr);            // 2^-g_r
                     km[e] = kv[e] * e1;
                     qm[e] = qv[e] * e1;
                     kh[e] = kv[e] * e2;
@@ -511,7 +492,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         tmem_wait_st();
     }
     tc_fence_before_sync();
-    __syncthreads();                  // K^m (or g) no longer needed
+    __syncthreads();                  // K^ (or g) no longer needed
     tc_fence_after_sync();
     abort = s_flag[1] != 0;
 
@@ -556,15 +537,15 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     inv_block<1>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
     inv_block<0>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
 
-    // ---- MMA-b: Y^ [K~m | V] -> [[W Em^-1, U0], [P T K~m, O0]].  K-steps 3..1
-    // of the [K~m] half were issued during the solve, as each block of Y^ was
+    // ---- MMA-b: Y^ [K~ | V] -> [[W, U0], [P T K~, O0]].  K-steps 3..1
+    // of the [K~] half were issued during the solve, as each block of Y^ was
     // stored; here the last one and the [V] half, whose issuing thread waits
     // for the V tile first (the MMA reads it).
     if (tid == 0 && !abort && !mbar_wait(&bars[0], 0, kWaitNs)) { s_flag[1] = 1; abort = true; }
     if (tid == 0 && !abort) {
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
         mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kY)),
-                    sdesc(smem_u32(sm + SmemA::kOpA), 16384, 1024, 2), id, true);   // last K-step of the [K~m] half
+                    sdesc(smem_u32(sm + SmemA::kOpA), 16384, 1024, 2), id, true);   // last K-step of the [K~] half
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
             mma_bf16_ss(tmem + 128, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
@@ -585,7 +566,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         const int quarter = warp & 3, half = warp >> 2;
         const int i = (quarter & 1) * 32 + lane;      // token row within the chunk
         const bool top = quarter < 2;
-        uint8_t* a1 = sm + SmemA::kOpA;               // [W; Q'] image, in place over [K~m; Q~m]
+        uint8_t* a1 = sm + SmemA::kOpA;               // [W; Q'] image, in place over [K~; Q~]
         const uint8_t* qm = sm + SmemA::kOpA;
 #pragma unroll 1
         for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
@@ -594,21 +575,16 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             tmem_wait_ld();
             const uint32_t kb = c0 >> 6, kin = c0 & 63;
             const int row = top ? i : 64 + i;
-            if (!top) {                                // Q' = (Q~m - P T K~m) Em
+            if (!top) {                                // Q' = Q~ - P T K~
                 float q0[8], q1[8];
                 unpack8(*(const uint4*)(qm + kb * 16384 + sw128_off(row, kin)), q0);
                 unpack8(*(const uint4*)(qm + kb * 16384 + sw128_off(row, kin + 8)), q1);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) { f[e] = q0[e] - f[e]; f[8 + e] = q1[e] - f[8 + e]; }
             }
-            float lo[8], hi[8], em[16];
+            float lo[8], hi[8];
 #pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
-                const float4 m = ((const float4*)(s_em + c0))[e4];
-                em[4 * e4] = m.x; em[4 * e4 + 1] = m.y; em[4 * e4 + 2] = m.z; em[4 * e4 + 3] = m.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { lo[e] = f[e] * em[e]; hi[e] = f[8 + e] * em[8 + e]; }
+            for (int e = 0; e < 8; ++e) { lo[e] = f[e]; hi[e] = f[8 + e]; }
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin)) = pack8(lo);
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = pack8(hi);
         }
