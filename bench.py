@@ -635,6 +635,24 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
         b.record(stream)
         torch.cuda.synchronize()
         link[name] = round(probe.numel() * probe.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+    # Both directions at once, as the pipeline runs them (H2D of q into dx["q"],
+    # D2H of dx["k"] into hx["k"]: each buffer receives its own bytes back).
+    pk = hx["k"].view(-1)[: probe.numel()]
+    dk = dx["k"].view(-1)[: probe.numel()]
+    a, b = make_events(2)
+    torch.cuda.synchronize()
+    a.record(stream)
+    h2d_s.wait_stream(stream)
+    d2h_s.wait_stream(stream)
+    with torch.cuda.stream(h2d_s):
+        dprobe.copy_(probe, non_blocking=True)
+    with torch.cuda.stream(d2h_s):
+        pk.copy_(dk, non_blocking=True)
+    stream.wait_stream(h2d_s)
+    stream.wait_stream(d2h_s)
+    b.record(stream)
+    torch.cuda.synchronize()
+    link["both_ways_gbs"] = round(2 * probe.numel() * probe.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
     steps = max(1, args.e2e_steps)
     t0, t1 = make_events(2)
     torch.cuda.synchronize()
