@@ -861,6 +861,18 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                 }
                 mma_commit(mbar);
             }
+            // Output pass: this thread's U0 (U warps) or O0 (O warps) pieces are
+            // read while MMA1 runs (the stage has landed).
+            uint4 pre[kOut ? 4 : 1];
+            if (kOut) {
+                const uint8_t* src = st + (q < 2 ? L::kU0 : L::kO0) + tok * (kTile * 2);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint8_t* p = src + ((col0 + 16 * hh) >> 4) * TcRec::kTileBytes;
+                    pre[2 * hh] = *(const uint4*)p;
+                    pre[2 * hh + 1] = *(const uint4*)(p + 16);
+                }
+            }
             good = good && mbar_wait(mbar, ph & 1, kWaitNs);
             ++ph;
             tc_fence_after_sync();
@@ -878,10 +890,15 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                     const int c = col0 + j2 + 16 * hh;
                     float lo[8], hi[8];
                     if (c < kTcD) {
-                        const uint8_t* u0 = st + L::kU0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2);
                         float a[8], b[8];
-                        unpack8(*(const uint4*)u0, a);
-                        unpack8(*(const uint4*)(u0 + 16), b);
+                        if (kOut) {
+                            unpack8(pre[2 * (j2 / 16 + hh)], a);
+                            unpack8(pre[2 * (j2 / 16 + hh) + 1], b);
+                        } else {
+                            const uint8_t* u0 = st + L::kU0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2);
+                            unpack8(*(const uint4*)u0, a);
+                            unpack8(*(const uint4*)(u0 + 16), b);
+                        }
 #pragma unroll
                         for (int e = 0; e < 8; ++e) { lo[e] = a[e] - d[e]; hi[e] = b[e] - d[8 + e]; }
                     } else {
@@ -912,10 +929,9 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                   for (int hh = 0; hh < kLdB; ++hh) {
                     const float (&d)[16] = dd[hh];
                     const int c = col0 + j2 + 16 * hh;
-                    const uint8_t* o0 = st + L::kO0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2);
                     float a[8], b[8];
-                    unpack8(*(const uint4*)o0, a);
-                    unpack8(*(const uint4*)(o0 + 16), b);
+                    unpack8(pre[2 * (j2 / 16 + hh)], a);
+                    unpack8(pre[2 * (j2 / 16 + hh) + 1], b);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) { a[e] += d[e]; b[e] += d[8 + e]; }
                     if (full) {
