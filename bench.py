@@ -653,6 +653,17 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
     b.record(stream)
     torch.cuda.synchronize()
     link["both_ways_gbs"] = round(2 * probe.numel() * probe.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+    # Each input copied whole (host to device), to show whether some of the
+    # pinned host memory is slower than the 1 GiB probed above.
+    per = {}
+    for n in NAMES:
+        a, b = make_events(2)
+        a.record(stream)
+        dx[n].copy_(hx[n], non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        per[n] = round(hx[n].numel() * hx[n].element_size() / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+    link["h2d_gbs_whole_inputs"] = per
     steps = max(1, args.e2e_steps)
     t0, t1 = make_events(2)
     torch.cuda.synchronize()
