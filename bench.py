@@ -581,9 +581,15 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
     h2d = sum(hx[n].numel() * hx[n].element_size() for n in NAMES) + hs0.numel() * 4
     d2h = hout.numel() * hout.element_size() + hsf.numel() * 4 + hho.numel() * hho.element_size()
 
+    spans = []                             # (first H2D start, last H2D end) events per step
+    # events for those spans, created (and synchronised) before anything is timed
+    span_pool = iter([make_events(2) for _ in range(2 + max(1, args.e2e_steps))])
+
     def step():
         h2d_s.wait_stream(stream)          # the previous step no longer reads the device inputs
+        e_h0, e_h1 = next(span_pool)
         with torch.cuda.stream(h2d_s):
+            e_h0.record(h2d_s)
             dst.copy_(hs0, non_blocking=True)
         ev_in, ev_out = [], []
         for k in range(pieces):
@@ -594,6 +600,8 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
                 e = torch.cuda.Event()
                 e.record(h2d_s)
                 ev_in.append(e)
+        e_h1.record(h2d_s)
+        spans.append((e_h0, e_h1))
         for k in range(pieces):
             a, b = k * tp, (k + 1) * tp
             stream.wait_event(ev_in[k])
@@ -675,6 +683,8 @@ def bench_e2e(kda, args, dev, stream, x, s0, w, desc, hand, ddesc):
     torch.cuda.synchronize()
     wall = (time.perf_counter() - w0) / steps
     ms = t0.elapsed_time(t1) / steps
+    h2d_ms = statistics.mean(a.elapsed_time(b) for a, b in spans[-steps:])
+    link["h2d_gbs_in_timed_steps"] = round(h2d / (h2d_ms * 1e-3) / 1e9, 1)
     return {"value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "wall_ms_per_step": round(wall * 1e3, 3),
             "steps": steps, "host_buffers": "pinned", "link_probe": link,
