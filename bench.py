@@ -195,13 +195,13 @@ def bench_workload(args):
     return w
 
 
-def prefill_launches(N, H, T, C=64, plan_sms=152, min_seg=128):
+def prefill_launches(N, H, T, C=64, plan_sms=152, min_seg=8):
     """Kernels one bf16 d=128 prefill launches: the sequence table, the
     intra-chunk kernel, the first chain launch, and -- when a sequence is long
     enough to be cut into segments -- the state scan (three or more segments)
     and the output passes of the later segments.  Mirrors the library's plan:
     (N * H) x (segments - 1) CTAs near the SM count, segment 0 about 1.3x the
-    others, at least 128 chunks each."""
+    others, at least 8 chunks each."""
     chunks = -(-T // C)
     target = plan_sms // max(1, N * H)
     if target < 2 or chunks <= 2 * min_seg:
@@ -342,6 +342,10 @@ def run_ours(args, dist: Dist):
     # --- the same prefill filling a prefix cache (state snapshots)
     if not args.no_snapshots:
         res["snapshots"] = bench_snapshots(kda, args, dev, stream, x, s0, out, sf, ws, w, peaks, peak_src, ms_step)
+
+    # --- prefill on the smaller workloads (0: fp32 d = 64, 1: 4,096 tokens, 2: varlen)
+    if not args.no_configs:
+        res["workloads"] = bench_configs(kda, args, dev, stream, peaks, peak_src)
 
     # --- reverse mode of the prefill (training), on the 4,096-token workload
     if not args.no_backward:
@@ -505,6 +509,65 @@ def bench_backward(kda, args, dev, stream, peaks, peak_src):
                          "algorithmic_per_launch": flop, "launch_ms": round(ms, 4)},
             "note": "fp32 CUDA cores, one CTA per (sequence, head, 8/16/32 state columns: the widest tile "
                     "that still fills the SMs); gradients of q, k, v, log_alpha, beta and the initial state"}
+
+
+def bench_configs(kda, args, dev, stream, peaks, peak_src, indices=(0, 1, 2)):
+    """Prefill throughput on the smaller workloads (0: one fp32 sequence, d = 64,
+    on the CUDA-core path; 1: 4,096 tokens x 16 heads; 2: the 8-sequence varlen
+    batch x 32 heads): tokens/s per call, the two kernels' times, and kernel (a)
+    against HBM on its input bytes.  Their inputs fit in L2, so a buffer twice
+    its size is written before every timed call (outside the call's events)."""
+    import ctypes
+    res = {}
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8, device=dev)
+    steps = 10
+    for idx in indices:
+        w = workload(idx)
+        T, H, D, Dv, N = w.total_tokens, w.num_heads, w.d_k, w.d_v, w.num_seqs
+        x = prefill_inputs(w, device=dev)
+        o = torch.empty((T, H, Dv), dtype=w.torch_dtype, device=dev)
+        sf = torch.empty((N, H, D, Dv), dtype=torch.float32, device=dev)
+        desc = kda.make_desc(N, H, D, Dv, T, w.torch_dtype)
+        ws = torch.empty(kda.kda_prefill_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+        desc = kda.make_desc(N, H, D, Dv, T, w.torch_dtype, ws)
+        call = (x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"], x["initial_state"], o, sf)
+        for _ in range(3):
+            rc = kda.kda_prefill(desc, *call, stream)
+            if rc:
+                raise kda.KdaError("kda_prefill", rc)
+        ev = [make_events(5) for _ in range(steps)]
+        keep = []
+        torch.cuda.synchronize()
+        for e in ev:
+            flush.zero_()
+            arr = (ctypes.c_void_p * 3)(*[x_.cuda_event for x_ in e[1:4]])
+            keep.append(arr)
+            desc.phase_events = ctypes.cast(arr, ctypes.c_void_p)
+            e[0].record(stream)
+            rc = kda.kda_prefill(desc, *call, stream)
+            e[4].record(stream)
+            if rc:
+                raise kda.KdaError("kda_prefill", rc)
+        torch.cuda.synchronize()
+        desc.phase_events = None
+        if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
+            raise RuntimeError(f"device status not OK (workload {idx})")
+        ms = statistics.mean(e[0].elapsed_time(e[4]) for e in ev)
+        intra = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        chain = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+        esz = 2 if w.dtype == "bf16" else 4
+        in_b = (4 * D + 1) * esz if Dv == D else (3 * D + Dv + 1) * esz
+        tc = w.dtype == "bf16" and D == 128
+        res[str(idx)] = {"workload": w.name, "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s",
+                         "ms_per_call": round(ms, 4), "intra_ms": round(intra, 4), "chain_ms": round(chain, 4),
+                         "path": "tensor cores" if tc else "CUDA cores (fp32)", "steps": steps,
+                         "roofline": hbm_roofline("kda intra-chunk (a)" + ("" if tc else ", CUDA cores"),
+                                                  T * H * in_b, intra, peaks, peak_src),
+                         "l2": "flushed before each call"}
+        del x, o, sf, ws
+    del flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def bench_decode(kda, args, dev, stream, peaks, peak_src):
@@ -786,6 +849,7 @@ def main():
     ap.add_argument("--no-scalar-gate", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-snapshots", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

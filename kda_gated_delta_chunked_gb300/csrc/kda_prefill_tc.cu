@@ -647,19 +647,24 @@ struct ScanPlan {
     int len;          // chunks of every later segment
     int segs_max;     // segments of the longest possible sequence
 };
+// Shortest segment, in chunks.  Segments are as long as the SM count allows
+// (2,069 / 1,591 chunks on a 2^20-token sequence of 16 heads); the floor only
+// matters for short sequences, whose walk is a few steps per segment.
+constexpr int64_t kMinSegChunks = 8;
+
 static ScanPlan scan_plan(int N, int H, int64_t T) {
     ScanPlan p;
     const int64_t chunks_max = (T + kChunk - 1) / kChunk;
     const int64_t nh = (int64_t)N * H;
     const int64_t target = nh > 0 ? kPlanSMs / nh : 1;    // CTAs per (sequence, head) in launches 1 and 3
-    if (target < 2 || chunks_max <= 2 * 128) {
+    if (target < 2 || chunks_max <= 2 * kMinSegChunks) {
         p.len0 = (int)(chunks_max > 0 ? chunks_max : 1);
         p.len = 1;
         p.segs_max = 1;
         return p;
     }
     int64_t len = (10 * chunks_max + 10 * target + 12) / (10 * target + 13);   // chunks_max / (target + 1.3)
-    if (len < 128) len = 128;                      // short segments are not worth the extra passes
+    if (len < kMinSegChunks) len = kMinSegChunks;  // below this the launches and the scan cost more than they save
     int64_t len0 = (13 * len + 9) / 10;
     if (len0 + target * len < chunks_max) len0 = chunks_max - target * len;
     if (len0 > chunks_max) len0 = chunks_max;
