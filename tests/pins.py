@@ -385,8 +385,32 @@ def pin_backward_no_write(O):
     assert np.all(g["dk"] == 0.0) and np.all(g["dv"] == 0.0), "beta = 0 but k or v has a gradient"
 
 
+def pin_chunked_backward(O):
+    """The reverse mode of the chunk form (oracle/chunked.py: the gradients a
+    chunked backward computes, chunk by chunk through T = (I + A)^-1 Diag(beta),
+    W, U0, P and the decays) equals the token-by-token reverse mode, for chunk
+    sizes 1, 2, 16 and 64 with partial chunks, a ragged varlen batch, an
+    initial state, output and final-state gradients, and the scalar gate."""
+    rng = np.random.default_rng(RNG_SEED + 25)
+    q, k, v, la, b = _rand_case(rng, 150, 2, 5, 4)
+    cu = np.array([0, 1, 70, 150], dtype=np.int32)
+    s0 = rng.standard_normal((3, 2, 5, 4)) * 0.2
+    do = rng.standard_normal((150, 2, 4))
+    dfin = rng.standard_normal((3, 2, 5, 4))
+    ref = O.backward(q, k, v, la, b, cu, s0, do, dfin)
+    for c in (1, 2, 16, 64):
+        got = chunked.backward(q, k, v, la, b, cu, s0, do, dfin, chunk=c)
+        for key in ref:
+            _close(got[key], ref[key], 1e-12, f"chunked backward C={c} {key}")
+    las = la[:, :, 0].copy()
+    ref = O.backward(q, k, v, las, b, cu, s0, do, None)
+    got = chunked.backward(q, k, v, las, b, cu, s0, do, None, chunk=16)
+    for key in ref:
+        _close(got[key], ref[key], 1e-12, f"chunked backward, scalar gate, {key}")
+
+
 ALL_PINS = [pin_deltanet, pin_gated_deltanet, pin_scalar_gate, pin_no_write, pin_exact_overwrite,
             pin_closed_forms, pin_chunked_form, pin_continuation, pin_varlen_isolation,
             pin_mode_duality, pin_linearity, pin_exact_rational, pin_zero_state_default,
             pin_backward_finite_differences, pin_backward_across_checkpoints, pin_backward_scalar_gate,
-            pin_backward_no_write]
+            pin_backward_no_write, pin_chunked_backward]
