@@ -248,9 +248,11 @@ KDA_API int kda_get_device_status(const kda_desc *desc, kda_stream_t stream);
  *    larger than KDA_PREFILL_NOALLOC_SCRATCH_BYTES, for example more than about
  *    800 chunk-heads of 64 tokens on the bf16 head-size-128 path) are rejected
  *    with KDA_ERR_WORKSPACE before any GPU work.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *  - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *    host-side, no stream work) with the caller's device current, so a
+ *    context that was reset and re-created gets the new address.  The first
+ *    call in a context may make the runtime load the library's kernels
+ *    there: make it before any stream capture.
  *  - All calls on a device share the one array, which keeps the last call's
  *    contents (nothing in it needs to start at zero).  Calls whose GPU work
  *    may overlap -- different streams, or host threads without ordering --

@@ -12,27 +12,25 @@
 // used there and keeps it until the process exits.
 //
 // Host code cannot use the array's name as a device address (on the host it
-// only names a stand-in object), so the first call on each device asks the
-// runtime for the array's device address with cudaGetSymbolAddress, with that
-// device current, and caches it.  That first call should therefore come
-// before any stream capture.
+// only names a stand-in object), so every call asks the runtime for the
+// array's device address with cudaGetSymbolAddress, with the caller's device
+// current, and passes that address to the kernels.  The lookup is host-side
+// work with no stream operation; nothing is cached, so a context that was
+// destroyed and re-created (cudaDeviceReset) or a different context on the
+// same device gets its own address.  The first call in a context may make the
+// runtime load the library's kernels there, so make it before any stream
+// capture.
 //
 // Every call on a device shares the one array.  The prefill writes every byte
 // of scratch it later reads (status word, sequence table, per-chunk records),
 // so nothing has to start at zero and the previous call's leftovers are
 // harmless; but calls whose GPU work overlaps (different streams, or
 // different host threads, without ordering between them) race on the array.
-#include <mutex>
-
 #include "kda_common.cuh"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_kda_noalloc_scratch[KDA_PREFILL_NOALLOC_SCRATCH_BYTES];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_lookup_mutex;
-void* g_scratch_ptr[kMaxDevices];   // device address of the array, per device, once looked up
 
 }  // namespace
 
@@ -50,20 +48,8 @@ extern "C" int kda_prefill_noalloc(const kda_desc* desc, const void* q, const vo
                            stream);                  // let the regular checks name the problem
     if (need > (size_t)KDA_PREFILL_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED;
     void* ptr = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_lookup_mutex);
-        if (!g_scratch_ptr[dev]) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_kda_noalloc_scratch) != cudaSuccess || p == nullptr)
-                return KDA_ERR_CUDA;
-            g_scratch_ptr[dev] = p;
-        }
-        ptr = g_scratch_ptr[dev];
-    }
+    if (cudaGetSymbolAddress(&ptr, g_kda_noalloc_scratch) != cudaSuccess || ptr == nullptr) return KDA_ERR_CUDA;
     d.workspace = ptr;
     d.workspace_bytes = (size_t)KDA_PREFILL_NOALLOC_SCRATCH_BYTES;
     return kda_prefill(&d, q, k, v, log_alpha, beta, cu_seqlens, initial_state, out, final_state, stream);

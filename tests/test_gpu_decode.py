@@ -33,7 +33,7 @@ def test_workload3_decode_64_steps(kda):
             torch.cuda.synchronize()
             assert_parity(f"decode step {step}", host(o), ro, None, None, "bf16")
     torch.cuda.synchronize()
-    assert_parity("decode final", host(o), ro, host(s_gpu), s_ref, "bf16")
+    assert_parity("workload3 decode 256x32, after 64 steps", host(o), ro, host(s_gpu), s_ref, "bf16")
     assert rel_l2(host(s_gpu), s_ref) < 1e-4     # the fp32 state itself is far tighter
 
 
