@@ -159,16 +159,20 @@ def kda_prefill_backward(desc: KdaDesc, q, k, v, log_alpha, beta, cu_seqlens, in
 
 
 def prefill_backward(q, k, v, log_alpha, beta, cu_seqlens=None, initial_state=None, *, d_out,
-                     d_final_state=None, want_initial_grad: bool = True, workspace=None, stream=None):
+                     d_final_state=None, want_initial_grad: bool = True, workspace=None, stream=None,
+                     flags: int = 0):
     """Gradients of a loss through kda_prefill (fp32 tensors), given d_out and
-    optionally d_final_state.  A 2-D ``log_alpha`` selects the scalar gate.
+    optionally d_final_state.  A 2-D ``log_alpha`` selects the scalar gate;
+    ``flags=KDA_FLAG_CUDA_CORE_PREFILL`` selects the fp32 CUDA-core backward
+    where the tensor-core one would run (bf16, head size 128).
     Returns a dict: dq, dk, dv, dlog_alpha, dbeta, d_initial_state (or None)."""
     T, H, dk_ = q.shape
     dv_ = v.shape[2]
     N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     for name, t in (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta), ("d_out", d_out)):
         _check(t, name)
-    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    if log_alpha.dim() == 2:
+        flags |= KDA_FLAG_SCALAR_GATE
     f32 = dict(dtype=torch.float32, device=q.device)
     g = {"dq": torch.empty((T, H, dk_), **f32), "dk": torch.empty((T, H, dk_), **f32),
          "dv": torch.empty((T, H, dv_), **f32), "dlog_alpha": torch.empty(tuple(log_alpha.shape), **f32),

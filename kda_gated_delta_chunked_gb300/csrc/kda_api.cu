@@ -77,6 +77,7 @@ kda_sequence_table(const int32_t* __restrict__ cu_in, int N, int64_t T_tot, Devi
         const int bad = s_bad || total > chunks_ub;
         chunk_first[N] = (int32_t)min64(total, 0x7fffffffLL);
         hdr->total_chunks = bad ? 0 : (int32_t)total;
+        hdr->pad[kHdrSlowChunk] = 0;
         hdr->status = bad ? KDA_ERR_BAD_SEQLENS : KDA_OK;
     }
 }
@@ -284,18 +285,31 @@ int kda_prefill_snapshots(const kda_desc* d, const void* q, const void* k, const
                              num_snapshots, snapshot_at, snapshots, stream);
 }
 
-// Backward workspace: header, chunk table, kept states, per-tile partial sums.
+// Backward workspace: header, chunk table, then the CUDA-core backward's kept
+// states and per-tile partial sums.  On the tensor-core path the same region
+// (from ckpt_off) first holds the tensor-core backward's scratch; the
+// CUDA-core kernels run after it only as its fallback, when the tensor-core
+// kernels have returned without work, so the two uses may overlap.
 struct BwdLayout {
+    bool tc;               // tensor-core backward (bf16, head size 128)
     int64_t chunks_ub;
     size_t table_off, ckpt_off, part_off, total;
 };
+static bool bwd_uses_tc(const kda_desc* d) {
+    return d->dtype == KDA_BF16 && d->d_k == 128 && (d->flags & KDA_FLAG_CUDA_CORE_PREFILL) == 0;
+}
 static BwdLayout bwd_layout(const kda_desc* d) {
     BwdLayout L;
+    L.tc = bwd_uses_tc(d);
     L.chunks_ub = (d->total_tokens + kChunk - 1) / kChunk + d->num_seqs;
     L.table_off = sizeof(DeviceHeader);
     L.ckpt_off = align_up(L.table_off + ((size_t)d->num_seqs + 1) * sizeof(int32_t), 1024);
     L.part_off = align_up(L.ckpt_off + backward_ckpt_bytes(d->d_k, d->num_heads, L.chunks_ub), 1024);
     L.total = L.part_off + backward_part_bytes(d->num_seqs, d->d_k, d->num_heads, d->total_tokens);
+    if (L.tc) {
+        const size_t tc_end = L.ckpt_off + backward_tc_bytes(d->num_seqs, d->num_heads, d->total_tokens, L.chunks_ub);
+        if (tc_end > L.total) L.total = tc_end;
+    }
     return L;
 }
 
@@ -361,6 +375,11 @@ int kda_prefill_backward(const kda_desc* d, const void* q, const void* k, const 
     a.dq = dq; a.dk = dk; a.dv = dv; a.dla = dlog_alpha; a.dbeta = dbeta; a.ds0 = d_initial_state;
     a.hdr = hdr; a.chunk_first = chunk_first;
     a.ckpt = (float*)(ws + L.ckpt_off); a.part = (float*)(ws + L.part_off);
+    a.only_if_slow = 0;
+    if (L.tc) {
+        if ((e = backward_tc_launch(a, L.chunks_ub, ws + L.ckpt_off, s)) != cudaSuccess) return cuda_fail(e);
+        a.only_if_slow = 1;         // the CUDA-core kernels below return unless a chunk was too strong
+    }
     if ((e = backward_launch(a, s)) != cudaSuccess) return cuda_fail(e);
     return KDA_OK;
 }

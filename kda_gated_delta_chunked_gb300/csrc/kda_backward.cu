@@ -21,6 +21,12 @@
 // dlog_alpha and dbeta are sums over all columns, so each tile writes its
 // partial sums and a second kernel adds the tiles in a fixed order (no
 // atomics: the result is deterministic).
+//
+// This is the backward for fp32 inputs and head size 64, and the fallback of
+// the tensor-core backward (kda_backward_tc.cu) for calls where some chunk's
+// decay is too strong for the factorised chunk products: there it is launched
+// after the tensor-core kernels and runs only if the forward flagged such a
+// chunk (only_if_slow).
 #include "kda_common.cuh"
 #include "kda_paths.h"
 
@@ -109,11 +115,11 @@ kda_backward_tile(const T* __restrict__ q, const T* __restrict__ k, const T* __r
                   const int32_t* __restrict__ chunk_first, int H, int64_t T_tot,
                   const float* __restrict__ s0, const T* __restrict__ dout, const float* __restrict__ dfinal,
                   float* __restrict__ ckpt, float* __restrict__ part, float* __restrict__ dv,
-                  float* __restrict__ ds0) {
+                  float* __restrict__ ds0, int only_if_slow) {
     using SM = BwdSmem<D, COLS>;
     constexpr int RP = SM::kRP, RG = SM::kRG;
     constexpr int kTiles = D / COLS;
-    if (hdr->status != KDA_OK) return;
+    if (hdr->status != KDA_OK || (only_if_slow && hdr->pad[kHdrSlowChunk] == 0)) return;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SM& sm = *reinterpret_cast<SM*>(smem_raw);
     const int nh = blockIdx.x, tile = blockIdx.y, n = nh / H, h = nh % H;
@@ -232,9 +238,9 @@ template <int D>
 __global__ void __launch_bounds__(256)
 kda_backward_reduce(const float* __restrict__ part, const DeviceHeader* __restrict__ hdr, int64_t T_tot, int H,
                     int kTiles, int la_scalar, float* __restrict__ dq, float* __restrict__ dk,
-                    float* __restrict__ dla, float* __restrict__ dbeta) {
+                    float* __restrict__ dla, float* __restrict__ dbeta, int only_if_slow) {
     constexpr int W = 3 * D + 1;
-    if (hdr->status != KDA_OK) return;
+    if (hdr->status != KDA_OK || (only_if_slow && hdr->pad[kHdrSlowChunk] == 0)) return;
     const int64_t th = blockIdx.x;                    // (token, head)
     if (th >= T_tot * H) return;
     __shared__ float s_la[D];
@@ -282,11 +288,12 @@ static cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t stream) {
     kda_backward_tile<T, D, COLS><<<dim3((unsigned)a.N * a.H, D / COLS), kBwdThreads, smem, stream>>>(
         (const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.la, a.la_scalar, (const T*)a.beta, a.cu,
         (const DeviceHeader*)a.hdr, a.chunk_first, a.H, a.T, a.s0, (const T*)a.dout, a.dfinal, a.ckpt, a.part,
-        a.dv, a.ds0);
+        a.dv, a.ds0, a.only_if_slow);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.T > 0) {
         kda_backward_reduce<D><<<(unsigned)(a.T * a.H), 256, 0, stream>>>(
-            a.part, (const DeviceHeader*)a.hdr, a.T, a.H, D / COLS, a.la_scalar, a.dq, a.dk, a.dla, a.dbeta);
+            a.part, (const DeviceHeader*)a.hdr, a.T, a.H, D / COLS, a.la_scalar, a.dq, a.dk, a.dla, a.dbeta,
+            a.only_if_slow);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

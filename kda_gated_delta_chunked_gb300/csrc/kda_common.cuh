@@ -26,8 +26,14 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 struct DeviceHeader {
     int32_t status;        // kda_status recorded by the device
     int32_t total_chunks;  // sum over sequences of ceil(len / kChunk)
-    int32_t pad[62];       // keeps the chunk table 256-byte aligned
+    int32_t pad[62];       // keeps the chunk table 256-byte aligned (pad[0..1]: cu_seqlens of a
+                           // single sequence; pad[kHdrSlowChunk]: see below)
 };
+// pad[kHdrSlowChunk] is cleared by the sequence-table kernel and set to 1 by
+// the tensor-core intra-chunk kernel when some chunk's cumulative decay is
+// too strong for its factorised products (it then takes its slow path).  The
+// tensor-core backward reads it to hand such calls to the CUDA-core backward.
+constexpr int kHdrSlowChunk = 8;
 
 __device__ __forceinline__ void record_status(DeviceHeader* hdr, int code) {
     atomicCAS(&hdr->status, (int)KDA_OK, code);

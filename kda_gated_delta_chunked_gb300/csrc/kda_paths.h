@@ -1,6 +1,7 @@
 // kda_paths.h -- host-side entry points of the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -50,6 +51,8 @@ struct BackwardArgs {
     const int32_t* chunk_first;
     float* ckpt;                 // kept states, backward_ckpt_bytes
     float* part;                 // per-tile partial sums, backward_part_bytes
+    int only_if_slow;            // 1: the CUDA-core kernels run only when the header's slow-chunk
+                                 //    flag is set (fallback of the tensor-core backward)
 };
 size_t backward_ckpt_bytes(int d, int H, int64_t chunks_ub);
 size_t backward_part_bytes(int N, int d, int H, int64_t T);
@@ -67,5 +70,12 @@ cudaError_t prefill_simt_launch(const PrefillArgs& a, cudaStream_t stream);
 size_t tc_record_bytes();
 size_t tc_extra_bytes(int N, int H, int64_t T);
 cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stream);
+// Tensor map of a [T, H, 128] bf16 tensor with 64-token x 64-channel boxes of
+// one head, 128-byte swizzle (a canonical MN-major operand tile per box).
+bool tc_make_tile_map(CUtensorMap* m, const void* base, int64_t T, int H);
+
+// Tensor-core backward (kda_backward_tc.cu): bf16 inputs, head size 128.
+size_t backward_tc_bytes(int N, int H, int64_t T, int64_t chunks_ub);
+cudaError_t backward_tc_launch(const BackwardArgs& a, int64_t chunks_ub, void* region, cudaStream_t stream);
 
 }  // namespace kda

@@ -77,27 +77,16 @@
 #include "kda_common.cuh"
 #include "kda_paths.h"
 #include "kda_sm100.cuh"
+#include "kda_tc_record.cuh"
 
 namespace kda {
 
 using namespace sm100;
 
 constexpr int kTcD = 128;                // head size handled here
-constexpr int kTile = 16;                // columns per tile of the U0 / O0 record images
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMaxSpanLog2 = 100.f;    // fast path if max_c (-g_C) <= 100 (log2 units, from the chunk start)
-
-// Record of one (chunk, head), bytes.
-struct TcRec {
-    static constexpr uint32_t kA1 = 0;          // [W; Q'] image: 2 K-blocks x [128 rows x 128 B]
-    static constexpr uint32_t kKE = 32768;      // K^end image: token-major, 2 x [64 tok x 64 ch]
-    static constexpr uint32_t kU0 = 49152;      // U0: 8 tiles x [64 tokens x 16] bf16
-    static constexpr uint32_t kO0 = 65536;      // O0: same layout
-    static constexpr uint32_t kGam = 81920;     // Gamma: 128 fp32
-    static constexpr uint32_t kBytes = 82432;
-    static constexpr uint32_t kTileBytes = 64 * kTile * 2;
-};
+constexpr float kMaxSpanLog2 = kTcMaxSpanLog2;   // fast path if max_c (-g_C) <= 100 (log2 units, from the chunk start)
 
 size_t tc_record_bytes() { return TcRec::kBytes; }
 
@@ -395,6 +384,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         return;
     }
     const bool slow = s_flag[0] != 0;
+    if (slow && tid == 0) hdr->pad[kHdrSlowChunk] = 1;   // some chunk needs the slow path
     if (R == 0) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) ((float*)(rec + TcRec::kGam))[8 * C + e] = exp2f(gC[e]);
@@ -1129,6 +1119,8 @@ static bool make_v_map(CUtensorMap* m, const void* base, int64_t T, int H) {
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+bool tc_make_tile_map(CUtensorMap* m, const void* base, int64_t T, int H) { return make_v_map(m, base, T, H); }
 
 cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stream) {
     cudaError_t e;
