@@ -462,53 +462,83 @@ def fp32_alu_peak(peaks):
     return p.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
 
 
+# Contractions of the chunked reverse mode per token*head (chunk C, head size
+# d), counted as the tensor cores issue them on the rows that carry results:
+# the forward recomputation (its dense-as-issued count, 180,224 at C=64,
+# d=128), the reverse chain over chunks (K^end dS' and [W; Q']^T [-K^end dS';
+# dO]: 6 d^2) and the per-chunk gradient products: G and Q~K^^T (4 C d),
+# T [K~ | V] (4 C d), W S (2 d^2), K^end dS' + P^T dO (2 d^2 + 2 C d),
+# U dS'^T (2 d^2), [dO; dU] S^T (4 d^2), dO U^T (2 C d), dW K~^T + dU V^T
+# (4 C d), T^T dU and T^T dW (4 C d), [dP; dG] K^ (4 C d), dP^T Q~ + dG^T K~
+# (4 C d).  The fp32 64 x 64 products behind dA and the solve are not counted.
+def backward_tc_flop_per_token(C=64, d=128):
+    fwd = dense_issued_flops(C, d)
+    chain = 6 * d * d
+    chunk = 28 * C * d + 10 * d * d
+    return fwd + chain + chunk
+
+
 def bench_backward(kda, args, dev, stream, peaks, peak_src):
-    """Prefill reverse mode (CUDA cores, fp32) on workload 1: tokens/s, and the
-    CUDA-core roofline on 20 d^2 FLOP per token and head (one forward step,
-    5 d^2, and its reverse, 15 d^2; the recomputation is not counted)."""
+    """Prefill reverse mode on workload 1: tokens/s of the tensor-core backward
+    (forward recomputation saving every chunk's state, the reverse chain, the
+    per-chunk gradient kernel) against the burst bf16 peak on its contraction
+    FLOPs, with the fp32 CUDA-core backward timed beside it."""
     w = workload(1)
     T, H, D = w.total_tokens, w.num_heads, w.d_k
     x = prefill_inputs(w, device=dev)
     gen = torch.Generator(device=dev).manual_seed(7)
     do = torch.randn((T, H, D), generator=gen, device=dev, dtype=torch.float32).to(w.torch_dtype)
     dfin = torch.randn((1, H, D, D), generator=gen, device=dev, dtype=torch.float32)
-    desc = kda.make_desc(1, H, D, D, T, w.torch_dtype)
-    ws = torch.empty(kda.kda_backward_workspace_bytes(desc), dtype=torch.uint8, device=dev)
-    desc = kda.make_desc(1, H, D, D, T, w.torch_dtype, ws)
     f32 = dict(dtype=torch.float32, device=dev)
     g = [torch.empty((T, H, D), **f32) for _ in range(4)] + [torch.empty((T, H), **f32),
                                                              torch.empty((1, H, D, D), **f32)]
 
-    def run():
-        rc = kda.kda_prefill_backward(desc, x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None,
-                                      x["initial_state"], do, dfin, *g, stream)
-        if rc:
-            raise kda.KdaError("kda_prefill_backward", rc)
+    def timed(flags):
+        desc = kda.make_desc(1, H, D, D, T, w.torch_dtype, flags=flags)
+        ws = torch.empty(kda.kda_backward_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+        desc = kda.make_desc(1, H, D, D, T, w.torch_dtype, ws, flags=flags)
 
-    for _ in range(2):
-        run()
-    steps = 3
-    t0, t1 = make_events(2)
-    torch.cuda.synchronize()
-    t0.record(stream)
-    for _ in range(steps):
-        run()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
-        raise RuntimeError("device status not OK (backward)")
-    ms = t0.elapsed_time(t1) / steps
-    flop = 20 * D * D * T * H
-    peak = fp32_alu_peak(peaks)
+        def run():
+            rc = kda.kda_prefill_backward(desc, x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None,
+                                          x["initial_state"], do, dfin, *g, stream)
+            if rc:
+                raise kda.KdaError("kda_prefill_backward", rc)
+
+        for _ in range(max(2, args.warmup)):
+            run()
+        steps = 5
+        t0, t1 = make_events(2)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(steps):
+            run()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if kda.kda_get_device_status(desc, stream) != kda.KDA_OK:
+            raise RuntimeError("device status not OK (backward)")
+        del ws
+        return t0.elapsed_time(t1) / steps, steps
+
+    ms, steps = timed(0)
+    ms_cc, _ = timed(kda.KDA_FLAG_CUDA_CORE_PREFILL)
+    per_tok = backward_tc_flop_per_token(64, D)
+    flop = per_tok * T * H
+    peak = peaks["bf16_tflops"]
     ach = flop / (ms * 1e-3) / 1e12
+    # sequence table, slot table, forward (intra + chain launches), reverse chain,
+    # per-chunk kernel, and the CUDA-core fallback's two launches (which return at once)
+    launches = 2 + (prefill_launches(1, H, T) - 1) + 2 + 2
     return {"workload": w.name, "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s",
-            "ms_per_step": round(ms, 3), "steps": steps, "gpu_launches": 3 * steps,
-            "roofline": {"bound": "alu", "achieved": round(ach, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
-                         "frac": round(ach / peak, 4), "traffic": None, "kernel": "kda backward (CUDA cores)",
-                         "peak_source": f"SMs x 128 fp32 lanes x 2 x {peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
-                         "algorithmic_per_launch": flop, "launch_ms": round(ms, 4)},
-            "note": "fp32 CUDA cores, one CTA per (sequence, head, 8/16/32 state columns: the widest tile "
-                    "that still fills the SMs); gradients of q, k, v, log_alpha, beta and the initial state"}
+            "ms_per_step": round(ms, 4), "steps": steps, "gpu_launches": launches * steps,
+            "path": "tensor cores (bf16 operands, fp32 accumulation)",
+            "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(ach / peak, 4), "traffic": None,
+                         "kernel": "kda backward, whole call (forward recompute + reverse chain + per-chunk gradients)",
+                         "peak_source": f"{peak_src} (bf16 burst)", "algorithmic_per_launch": flop,
+                         "flop_per_token_head": per_tok, "launch_ms": round(ms, 4)},
+            "cuda_core": {"ms_per_step": round(ms_cc, 4), "value": round(T / (ms_cc * 1e-3), 1),
+                          "unit": "tokens/s", "speedup_of_tensor_cores": round(ms_cc / ms, 2)},
+            "note": "gradients of q, k, v, log_alpha, beta and the initial state"}
 
 
 def bench_configs(kda, args, dev, stream, peaks, peak_src, indices=(0, 1, 2)):
