@@ -880,6 +880,8 @@ def main():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-snapshots", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the prefill's reverse mode (workload 1) and print its JSON object")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -889,6 +891,13 @@ def main():
         if rank != 0:
             return
         print(json.dumps(run_reference(args)))
+        return
+    if args.backward_only:
+        import kda_gated_delta_chunked_gb300 as kda
+        torch.cuda.set_device(0)
+        peaks, peak_src = load_peaks()
+        print(json.dumps(bench_backward(kda, args, torch.device("cuda", 0), torch.cuda.current_stream(), peaks,
+                                        peak_src)))
         return
     dist = Dist()
     try:

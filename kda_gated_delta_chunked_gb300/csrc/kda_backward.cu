@@ -241,27 +241,28 @@ kda_backward_reduce(const float* __restrict__ part, const DeviceHeader* __restri
                     float* __restrict__ dla, float* __restrict__ dbeta, int only_if_slow) {
     constexpr int W = 3 * D + 1;
     if (hdr->status != KDA_OK || (only_if_slow && hdr->pad[kHdrSlowChunk] == 0)) return;
-    const int64_t th = blockIdx.x;                    // (token, head)
-    if (th >= T_tot * H) return;
     __shared__ float s_la[D];
-    for (int w = threadIdx.x; w < W; w += blockDim.x) {
-        float acc = 0.f;
-        for (int tl = 0; tl < kTiles; ++tl) acc += part[((size_t)tl * T_tot * H + th) * W + w];
-        const int m = w / D, i = w % D;
-        if (w == 3 * D) dbeta[th] = acc;
-        else if (m == 0) dq[th * D + i] = acc;
-        else if (m == 1) dk[th * D + i] = acc;
-        else if (la_scalar) s_la[i] = acc;
-        else dla[th * D + i] = acc;
-    }
-    if (la_scalar) {
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            float a = 0.f;
-            for (int i = threadIdx.x; i < D; i += 32) a += s_la[i];
+    for (int64_t th = blockIdx.x; th < T_tot * H; th += gridDim.x) {   // (token, head)
+        for (int w = threadIdx.x; w < W; w += blockDim.x) {
+            float acc = 0.f;
+            for (int tl = 0; tl < kTiles; ++tl) acc += part[((size_t)tl * T_tot * H + th) * W + w];
+            const int m = w / D, i = w % D;
+            if (w == 3 * D) dbeta[th] = acc;
+            else if (m == 0) dq[th * D + i] = acc;
+            else if (m == 1) dk[th * D + i] = acc;
+            else if (la_scalar) s_la[i] = acc;
+            else dla[th * D + i] = acc;
+        }
+        if (la_scalar) {
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                float a = 0.f;
+                for (int i = threadIdx.x; i < D; i += 32) a += s_la[i];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (threadIdx.x == 0) dla[th] = a;
+                for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                if (threadIdx.x == 0) dla[th] = a;
+            }
+            __syncthreads();
         }
     }
 }
@@ -291,7 +292,8 @@ static cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t stream) {
         a.dv, a.ds0, a.only_if_slow);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.T > 0) {
-        kda_backward_reduce<D><<<(unsigned)(a.T * a.H), 256, 0, stream>>>(
+        const int64_t rows = a.T * a.H;
+        kda_backward_reduce<D><<<(unsigned)(rows < 16384 ? rows : 16384), 256, 0, stream>>>(
             a.part, (const DeviceHeader*)a.hdr, a.T, a.H, D / COLS, a.la_scalar, a.dq, a.dk, a.dla, a.dbeta,
             a.only_if_slow);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

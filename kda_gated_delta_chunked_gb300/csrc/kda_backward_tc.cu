@@ -71,6 +71,13 @@ __device__ __forceinline__ uint32_t pk2(float lo, float hi) {
 __device__ __forceinline__ uint4 pk8(const float* f) {
     return make_uint4(pk2(f[0], f[1]), pk2(f[2], f[3]), pk2(f[4], f[5]), pk2(f[6], f[7]));
 }
+// 2^x with the special-function unit's instruction; every argument here lies in
+// [-100, 100] (the chunks these kernels take have decays within 2^100).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float bflo(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float bfhi(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
 __device__ __forceinline__ void unpk8(const uint4& v, float* f) {
@@ -98,8 +105,8 @@ struct RcSmem {
     static constexpr uint32_t kDO = 49152;      // dO tile, 2 x [64 tok x 64 ch] (TMA)
     static constexpr uint32_t kGam = 65536;     // Gamma (512 B)
     static constexpr uint32_t kStage = 66560;   // per stage, 1024-aligned
-    static constexpr uint32_t kX = 2 * kStage;  // dS' as bf16, MN-major [128 x 128]
-    static constexpr uint32_t kNDV = kX + 32768;   // -K^end dS', MN-major [64 x 128]
+    static constexpr uint32_t kX = 2 * kStage;  // dS' as bf16, MN-major [128 x 128], two buffers
+    static constexpr uint32_t kNDV = kX + 65536;   // -K^end dS', MN-major [64 x 128]
     static constexpr uint32_t kMisc = kNDV + 16384;
     static constexpr uint32_t kBytes = kMisc + 256 + 1024;
     static constexpr uint32_t kTx = 32768 + 16384 + 16384 + 512;
@@ -115,7 +122,8 @@ struct RcArgs {
     int H;
     const uint8_t* recs;         // the forward's records
     const float* dfinal;         // dLoss / dfinal_state or null
-    float* dsend;                // [chunks, H, 128, 128] gradient of each chunk's end state
+    uint8_t* dsend;              // [chunks, H] gradient of each chunk's end state, bf16 operand tiles
+                                 //   (128 x 128, two 64-column atoms of 128 rows, 128-byte swizzle)
     float* ds0;                  // dLoss / dinitial_state or null
 };
 
@@ -191,16 +199,16 @@ __global__ void __launch_bounds__(kRcThreads, 1) kda_tc_bwd_chain(const __grid_c
 #pragma unroll
             for (int j = 0; j < 32; ++j) X[j] = 0.f;
         }
-        uint8_t* XO = sm + RcSmem::kX;
         uint8_t* NDV = sm + RcSmem::kNDV;
-        auto write_X = [&]() {
+        auto write_X = [&](int b) {
+            uint8_t* XO = sm + RcSmem::kX + b * 32768;
 #pragma unroll
             for (int j = 0; j < 32; j += 8) *(uint4*)(XO + toff(i, col0 + j, 128)) = pk8(&X[j]);
         };
         const uint32_t id1 = idesc_bf16(128, 128, 0, 1);
         const uint32_t id2 = idesc_bf16(128, 128, 1, 1);
         uint32_t ph = 0;
-        write_X();
+        write_X(0);
         fence_proxy_async_smem();
         tc_fence_before_sync();
         bool ok = bar_and(32 * kRcWarps, true);
@@ -208,6 +216,13 @@ __global__ void __launch_bounds__(kRcThreads, 1) kda_tc_bwd_chain(const __grid_c
             const int s = it & 1;
             const int c = c_seq + nch - 1 - it;
             const uint8_t* st = sm + s * RcSmem::kStage;
+            uint8_t* XO = sm + RcSmem::kX + (it & 1) * 32768;     // dS' of this chunk, bf16
+            if (tid == 0) {
+                // the gradient of this chunk's end state, for the per-chunk kernel: the
+                // operand tile itself, stored by the bulk-copy engine while MMA-r1 reads it
+                bulk_s2g(A.dsend + ((size_t)c * H + h) * 32768, XO, 32768);
+                bulk_commit();
+            }
             bool good = mbar_wait(&full[s], (it >> 1) & 1, kWait);
             tc_fence_after_sync();
             if (tid == 0 && good) {
@@ -216,12 +231,6 @@ __global__ void __launch_bounds__(kRcThreads, 1) kda_tc_bwd_chain(const __grid_c
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16_ss(tmem, dk_(st + RcSmem::kKE, ks, 64), dmn(XO, ks, 16384), id1, ks > 0);
                 mma_commit(mbar);
-            }
-            // dS' of this chunk (the gradient of its end state), while MMA-r1 runs
-            {
-                float* dst = A.dsend + (((size_t)c * H + h) * kD + i) * kD + col0;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
             }
             good = good && mbar_wait(mbar, ph & 1, kWait);
             ++ph;
@@ -239,6 +248,8 @@ __global__ void __launch_bounds__(kRcThreads, 1) kda_tc_bwd_chain(const __grid_c
                 }
                 fence_proxy_async_smem();
             }
+            // the other dS' buffer is written below: its store (two chunks back) has read it
+            if (tid == 0) bulk_wait_read_1();
             tc_fence_before_sync();
             good = bar_and(32 * kRcWarps, good);
             tc_fence_after_sync();
@@ -263,12 +274,13 @@ __global__ void __launch_bounds__(kRcThreads, 1) kda_tc_bwd_chain(const __grid_c
 #pragma unroll
                 for (int e = 0; e < 16; ++e) X[j + e] = fmaf(gam, X[j + e], d[e]);
             }
-            write_X();
+            write_X((it + 1) & 1);
             fence_proxy_async_smem();
             tc_fence_before_sync();
             ok = bar_and(32 * kRcWarps, good);
             if (ok && tid == 0) mbar_arrive(&empty[s]);
         }
+        if (tid == 0) bulk_wait_all();
         if (!ok) {
             *(volatile int*)s_abort = 1;
             if (tid == 0) record_status(hdr, KDA_ERR_TIMEOUT);
@@ -293,12 +305,12 @@ struct PcSmem {
     static constexpr uint32_t kDD = 32768;      // [dO; dU] 128 x 128 (dO by TMA into rows 0..63)
     static constexpr uint32_t kSS = 65536;      // S 128 x 128; later dW (64 x 128), dP, dG (64 x 64 each);
                                                 //   at the end dg fp32 [64][128].  (Phase 0: prefix sums.)
-    static constexpr uint32_t kDS = 98304;      // A-bar fp32 [64][68] (solve), then dS' 128 x 128; later
+    static constexpr uint32_t kDS = 98304;      // M fp32 [64][64] (solve), then dS' 128 x 128; later
                                                 //   dT / dA fp32 [64][68], M fp32 [64][68], M^T fp32 [64][64],
                                                 //   X1 fp32 [64][64]; at the end g fp32 [64][128], dK~ fp32 [64][132]
     static constexpr uint32_t kVT = 131072;     // V 64 x 128 (TMA)
     static constexpr uint32_t kKE = 147456;     // K^end 64 x 128
-    static constexpr uint32_t kWU = 163840;     // -W, then U, 64 x 128
+    static constexpr uint32_t kWU = 163840;     // A-bar fp32 [64][64] (solve), then -W, then U, 64 x 128
     static constexpr uint32_t kZ0 = 180224;     // zeros 64 x 64 (the first M atom of [0; T^T])
     static constexpr uint32_t kTT = 188416;     // T 64 x 64
     static constexpr uint32_t kPT = 196608;     // P 64 x 64; later prefix sums, column partials
@@ -323,7 +335,7 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
                  const __nv_bfloat16* __restrict__ log_alpha, const __nv_bfloat16* __restrict__ beta,
                  const int32_t* __restrict__ cu, DeviceHeader* __restrict__ hdr,
                  const int32_t* __restrict__ chunk_first, int N, int H, const float* __restrict__ s0,
-                 const float* __restrict__ snaps, const float* __restrict__ dsend, float* __restrict__ dq,
+                 const float* __restrict__ snaps, const uint8_t* __restrict__ dsend, float* __restrict__ dq,
                  float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dla,
                  float* __restrict__ dbeta) {
     using L = PcSmem;
@@ -336,7 +348,7 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
     const int len = (int)min64(kChunk, (int64_t)cu[n + 1] - t0);
     const float* S_src = c > c_first ? snaps + ((size_t)(c - 1) * H + h) * kD * kD
                                      : (s0 ? s0 + ((size_t)n * H + h) * kD * kD : nullptr);
-    const float* dS_src = dsend + ((size_t)c * H + h) * kD * kD;
+    const uint8_t* dS_src = dsend + ((size_t)c * H + h) * 32768;   // bf16 operand tile of dS'
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -384,11 +396,13 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
     }
     __syncthreads();
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[0], 32768);
+        mbar_arrive_expect_tx(&bars[0], 32768 + 32768);
         tma_load_3d(sm + L::kVT, &tm_v, 0, h, (int)t0, &bars[0]);
         tma_load_3d(sm + L::kVT + 8192, &tm_v, 64, h, (int)t0, &bars[0]);
         tma_load_3d(sm + L::kDD, &tm_do, 0, h, (int)t0, &bars[0]);
         tma_load_3d(sm + L::kDD + 16384, &tm_do, 64, h, (int)t0, &bars[0]);
+        bulk_g2s(sm + L::kDS, dS_src, 32768, &bars[0]);
+        if (S_src) bulk_prefetch_l2(S_src, kD * kD * 4);
     }
     if (warp == 0) { tmem_alloc(s_tmem, 512); tmem_relinquish(); }
 
@@ -441,11 +455,11 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float g = part[e] + gl[i][e];
-                const float e1 = exp2f(g), e2 = exp2f(-g);
+                const float e1 = ex2(g), e2 = ex2(-g);
                 kt[e] = kv[e] * e1;
                 qt[e] = qv[e] * e1;
                 kh[e] = kv[e] * e2;
-                ke[e] = kv[e] * exp2f(s_gC[8 * C + e] - g);
+                ke[e] = kv[e] * ex2(s_gC[8 * C + e] - g);
             }
             *(uint4*)(sm + L::kKQ + toff(r, 8 * C, 128)) = pk8(kt);
             *(uint4*)(sm + L::kKQ + toff(64 + r, 8 * C, 128)) = pk8(qt);
@@ -473,7 +487,6 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
         __syncthreads();
         tc_fence_after_sync();
     };
-    const float* abar = (const float*)(sm + L::kDS);
     bool ok = true;
 
     // ---- phase 1: [K~; Q~] K^^T -> Gram G (rows 0..63) and Q~ K^^T (rows 64..127) ----
@@ -494,7 +507,7 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
             if (quarter < 2) {
                 const int i = 32 * quarter + lane;
                 const float bi = s_beta[i];
-                float* dst = (float*)(sm + L::kDS) + i * kLd + j0;
+                float* dst = (float*)(sm + L::kWU) + i * 64 + j0;
 #pragma unroll
                 for (int e4 = 0; e4 < 4; ++e4) {
                     float4 v;
@@ -517,19 +530,24 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
     }
     cta_sync();
 
-    // ---- phase 2: M (I + A-bar) = I, one row per thread (warps 0, 1), fp32;
-    //      meanwhile warps 2..5 convert S to bf16 ----
-    if (ok && warp < 2) {
-        const int r = tid;
-        float z[64];
+    // ---- phase 2: M = (I + A-bar)^-1 in fp32, by 16 x 16 blocks: the four
+    //      diagonal blocks D_i = (I + A-bar_ii)^-1 by a right-looking recursion
+    //      (one row per thread, warps 0, 1), then the blocks below the
+    //      diagonal, distance d = 1, 2, 3 in turn, from (I + A-bar) M = I:
+    //        M_ij = -D_i sum_{k=j}^{i-1} A-bar_ik M_kj   (all threads). ----
+    {
+        const float* Ab = (const float*)(sm + L::kWU);          // A-bar, [64][64]
+        float* Mw = (float*)(sm + L::kSS);                      // M, [64][64] (S is converted later)
+        float* Xs = Mw + 64 * 64;                               // block products, up to 3 x [16][16]
+        if (ok && warp < 2) {
+            const int bi = tid >> 4, rr = tid & 15, i = 16 * bi + rr;
+            float z[16];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) z[j] = (j == r) ? 1.f : 0.f;
-        const int mmax = warp == 0 ? 31 : 63;        // rows < 32 have M[r][m] = 0 for m > 31
+            for (int j = 0; j < 16; ++j) z[j] = (j == rr) ? 1.f : 0.f;
 #pragma unroll
-        for (int m = 63; m >= 1; --m) {
-            if (m <= mmax) {
+            for (int m = 15; m >= 1; --m) {
                 const float zm = z[m];
-                const float4* ar = (const float4*)(abar + m * kLd);
+                const float4* ar = (const float4*)(Ab + (16 * bi + m) * 64 + 16 * bi);
 #pragma unroll
                 for (int g4 = 0; 4 * g4 < m; ++g4) {
                     const float4 a = ar[g4];
@@ -539,37 +557,65 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
                     if (4 * g4 + 3 < m) z[4 * g4 + 3] = fmaf(-zm, a.w, z[4 * g4 + 3]);
                 }
             }
-        }
-        // M row r -> TMEM R0 columns 64..127 (lane r); T = M Diag(beta) -> bf16 tile
+            float* mrow = Mw + i * 64;
 #pragma unroll
-        for (int j = 0; j < 64; j += 16) {
-            float f[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) f[e] = z[j + e];
-            tmem_st16(tmem_addr(R0, 32 * warp, 64 + j), f);
-        }
-        tmem_wait_st();
-#pragma unroll
-        for (int j = 0; j < 64; j += 8) {
-            float t8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t8[e] = z[j + e] * s_beta[j + e];
-            *(uint4*)(sm + L::kTT + toff(r, j, 64)) = pk8(t8);
-        }
-    } else if (ok && warp < 6) {
-        const int i = tid - 64;                       // row of S
-        const float* src = S_src ? S_src + (size_t)i * kD : nullptr;
-#pragma unroll 4
-        for (int j = 0; j < kD; j += 8) {
-            float f[8];
-            if (src) {
-                const float4 a = *(const float4*)(src + j), b = *(const float4*)(src + j + 4);
-                f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            for (int c4 = 0; c4 < 16; ++c4) {
+                const int c = 4 * c4;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if ((c >> 4) == bi) v = make_float4(z[c & 15], z[(c & 15) + 1], z[(c & 15) + 2], z[(c & 15) + 3]);
+                *(float4*)(mrow + c) = v;
             }
-            *(uint4*)(sm + L::kSS + toff(i, j, 128)) = pk8(f);
+        }
+        __syncthreads();
+        for (int d = 1; d <= 3; ++d) {
+            const int ne = (4 - d) * 256;
+            if (ok) {
+                for (int e = tid; e < ne; e += kPcThreads) {
+                    const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15, i = b + d, j = b;
+                    const float* arow = Ab + (16 * i + r) * 64;
+                    float acc = 0.f;
+                    for (int kk = 16 * j; kk < 16 * i; kk += 4) {
+                        const float4 a = *(const float4*)(arow + kk);
+                        acc = fmaf(a.x, Mw[(kk + 0) * 64 + 16 * j + cc], acc);
+                        acc = fmaf(a.y, Mw[(kk + 1) * 64 + 16 * j + cc], acc);
+                        acc = fmaf(a.z, Mw[(kk + 2) * 64 + 16 * j + cc], acc);
+                        acc = fmaf(a.w, Mw[(kk + 3) * 64 + 16 * j + cc], acc);
+                    }
+                    Xs[e] = acc;
+                }
+            }
+            __syncthreads();
+            if (ok) {
+                for (int e = tid; e < ne; e += kPcThreads) {
+                    const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15, i = b + d, j = b;
+                    const float* drow = Mw + (16 * i + r) * 64 + 16 * i;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) acc = fmaf(drow[kk], Xs[(b << 8) + (kk << 4) + cc], acc);
+                    Mw[(16 * i + r) * 64 + 16 * j + cc] = -acc;
+                }
+            }
+            __syncthreads();
+        }
+        if (ok && warp < 2) {
+            // M row r -> TMEM R0 columns 64..127 (lane r); T = M Diag(beta) -> bf16 tile
+            const int r = tid;
+            const float* mrow = Mw + r * 64;
+#pragma unroll
+            for (int j = 0; j < 64; j += 16) {
+                float f[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) f[e] = mrow[j + e];
+                tmem_st16(tmem_addr(R0, 32 * warp, 64 + j), f);
+            }
+            tmem_wait_st();
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+                float t8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t8[e] = mrow[j + e] * s_beta[j + e];
+                *(uint4*)(sm + L::kTT + toff(r, j, 64)) = pk8(t8);
+            }
         }
     }
     fence_proxy_async_smem();
@@ -589,24 +635,35 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
         }
         mma_commit(&bars[1]);
     }
-    if (ok && warp >= 2 && warp < 6) {
-        // dS' -> bf16 tile (over A-bar, dead after the solve); dGamma_i = sum_j dS'_ij S_ij
-        const int i = tid - 64;
-        const float* src = dS_src + (size_t)i * kD;
-        const float* srs = S_src ? S_src + (size_t)i * kD : nullptr;
-        float acc = 0.f;
-#pragma unroll 4
-        for (int j = 0; j < kD; j += 8) {
-            const float4 a = *(const float4*)(src + j), b = *(const float4*)(src + j + 4);
-            float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            if (srs) {
-                const float4 x = *(const float4*)(srs + j), y = *(const float4*)(srs + j + 4);
-                acc += f[0] * x.x + f[1] * x.y + f[2] * x.z + f[3] * x.w + f[4] * y.x + f[5] * y.y + f[6] * y.z +
-                       f[7] * y.w;
-            }
-            *(uint4*)(sm + L::kDS + toff(i, j, 128)) = pk8(f);
+    if (ok) {
+        // S -> bf16 tile (over the solve's scratch); dGamma_i = sum_j dS'_ij S_ij with
+        // dS' from its bf16 tile (landed with the loads of phase 0).  Two threads per
+        // row of S, 64 columns each, every load issued first.
+        const int i = tid >> 1, c0 = 64 * (tid & 1);
+        float4 x[16];
+        if (S_src) {
+            const float4* srs = (const float4*)(S_src + (size_t)i * kD + c0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = srs[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        s_dgam[i] = acc;
+        const bool landed = mbar_wait(&bars[0], 0, kWait);
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float f[8] = {x[2 * j].x, x[2 * j].y, x[2 * j].z, x[2 * j].w,
+                                x[2 * j + 1].x, x[2 * j + 1].y, x[2 * j + 1].z, x[2 * j + 1].w};
+            *(uint4*)(sm + L::kSS + toff(i, c0 + 8 * j, 128)) = pk8(f);
+            float g8[8];
+            unpk8(*(const uint4*)(sm + L::kDS + toff(i, c0 + 8 * j, 128)), g8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(f[e], g8[e], acc);
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if ((tid & 1) == 0) s_dgam[i] = acc;
+        if (!landed) ok = false;
     }
     if (tid == 0 && !tma_done) ok = false;
     ok = mma_done(ok);
@@ -906,7 +963,7 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
     constexpr int kLdK = 132;
     float* dkt = (float*)(sm + L::kDKT);           // dK~ fp32 [64][132]
     float* dgs = (float*)(sm + L::kSS);            // dg fp32 [64][128]
-    float* s_kt = (float*)(sm + L::kZ0);           // [2][128] column partials of dK^end o K^end
+    float* kts = (float*)(sm + L::kKQ);            // dK^end o K^end fp32 [64][128] (over K~, Q~)
     if (ok && quarter >= 2) {
         const int r = 32 * (quarter - 2) + lane;
         const int64_t t = t0 + r;
@@ -951,25 +1008,23 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
                 }
                 unpk8(a, kv); unpk8(b, kv + 8); unpk8(c2, qv); unpk8(d2, qv + 8);
             }
-            float dkv[16], dqv[16], dgv[16];
+            float dkv[16], dqv[16], dgv[16], ktv[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const float g = gs[r * kD + j + e];
-                const float e1 = exp2f(g), e2 = exp2f(-g), e3 = exp2f(s_gC[j + e] - g);
+                const float e1 = ex2(g), e2 = ex2(-g), e3 = ex2(s_gC[j + e] - g);
                 const float dKt = dkt[r * kLdK + j + e];
                 const float a1 = dKt * e1, a2 = dKh[e] * e2, a3 = dKe[e] * e3, a4 = dQt[e] * e1;
                 dkv[e] = a1 + a2 + a3;
                 dqv[e] = a4;
                 dgv[e] = kv[e] * (a1 - a2 - a3) + qv[e] * a4;
-                // column partial of dK^end o K^end over this warp's 32 tokens
-                float kt = kv[e] * a3;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) kt += __shfl_xor_sync(0xffffffffu, kt, o);
-                if (lane == 0) s_kt[quarter * kD + j + e] = kt;
+                ktv[e] = kv[e] * a3;                       // dK^end o K^end
             }
 #pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4)
+            for (int e4 = 0; e4 < 4; ++e4) {
                 *(float4*)(dgs + r * kD + j + 4 * e4) = make_float4(dgv[4 * e4], dgv[4 * e4 + 1], dgv[4 * e4 + 2], dgv[4 * e4 + 3]);
+                *(float4*)(kts + r * kD + j + 4 * e4) = make_float4(ktv[4 * e4], ktv[4 * e4 + 1], ktv[4 * e4 + 2], ktv[4 * e4 + 3]);
+            }
             if (in) {
                 float* pk = dk + ((size_t)t * H + h) * kD + j;
                 float* pq = dq + ((size_t)t * H + h) * kD + j;
@@ -985,7 +1040,8 @@ kda_tc_bwd_chunk(const __grid_constant__ CUtensorMap tm_v, const __grid_constant
     if (ok && tid < kD) {
         // dlog alpha_r = sum_{r' >= r} dg_r' + colsum(dK^end o K^end) + dGamma Gamma, per channel
         const int ch = tid;
-        float acc = s_kt[ch] + s_kt[kD + ch] + s_dgam[ch] * exp2f(s_gC[ch]);
+        float acc = s_dgam[ch] * ex2(s_gC[ch]);
+        for (int r = 0; r < kChunk; ++r) acc += kts[r * kD + ch];     // (zero on padding rows)
         for (int r = len - 1; r >= 0; --r) {
             acc += dgs[r * kD + ch];
             if (kScalarGate) dgs[r * kD + ch] = acc;
@@ -1018,8 +1074,9 @@ __global__ void kda_tc_bwd_slots(int32_t* __restrict__ slot, int64_t n) {
 // Host side
 // ---------------------------------------------------------------------------
 // Scratch of the tensor-core backward, in order: snapshot slot per chunk, the
-// forward's records and segment scratch, every chunk's end state, every
-// chunk's end-state gradient, and the forward's (unused) outputs.
+// forward's records and segment scratch, every chunk's end state (fp32), every
+// chunk's end-state gradient (a bf16 operand tile), and the forward's (unused)
+// outputs.
 struct TcBwdLayout {
     size_t slot, recs, extra, snaps, dsend, out, total;
 };
@@ -1032,7 +1089,7 @@ static TcBwdLayout tc_bwd_layout(int N, int H, int64_t T, int64_t chunks_ub) {
     L.extra = al1k(L.recs + (size_t)chunks_ub * H * TcRec::kBytes);
     L.snaps = al1k(L.extra + tc_extra_bytes(N, H, T));
     L.dsend = al1k(L.snaps + (size_t)chunks_ub * H * st);
-    L.out = al1k(L.dsend + (size_t)chunks_ub * H * st);
+    L.out = al1k(L.dsend + (size_t)chunks_ub * H * (st / 2));
     L.total = al1k(L.out + (size_t)T * H * kD * 2);
     return L;
 }
@@ -1047,7 +1104,7 @@ cudaError_t backward_tc_launch(const BackwardArgs& a, int64_t chunks_ub, void* r
     uint8_t* base = (uint8_t*)region;
     int32_t* slot = (int32_t*)(base + L.slot);
     float* snaps = (float*)(base + L.snaps);
-    float* dsend = (float*)(base + L.dsend);
+    uint8_t* dsend = base + L.dsend;
     if (chunks_ub > 0) {
         kda_tc_bwd_slots<<<(unsigned)((chunks_ub + 255) / 256), 256, 0, stream>>>(slot, chunks_ub);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
