@@ -663,9 +663,11 @@ static ScanPlan scan_plan(int N, int H, int64_t T) {
     p.segs_max = chunks_max <= len0 ? 1 : 1 + (int)((chunks_max - len0 + len - 1) / len);
     return p;
 }
-// Segment scratch per (sequence, head, segment): [B_p | M_p] fp32 [128][256] and
+// Segment scratch per (sequence, head, segment): M_p fp32 [128][128] (contiguous,
+// so that the scan moves it with one bulk copy), B_p fp32 [128][128], and
 // S_start fp32 [128][128].
-constexpr size_t kSegMB = (size_t)kTcD * 256 * 4, kSegS = (size_t)kTcD * kTcD * 4, kSegBytes = kSegMB + kSegS;
+constexpr size_t kSegM = 0, kSegB = (size_t)kTcD * kTcD * 4, kSegMB = 2 * kSegB;
+constexpr size_t kSegS = (size_t)kTcD * kTcD * 4, kSegBytes = kSegMB + kSegS;
 
 // Number of segments of a sequence of nch chunks, and the first chunk of segment p.
 __host__ __device__ __forceinline__ int seg_count(int nch, int len0, int len) {
@@ -1012,7 +1014,8 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                 for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
             }
         } else {
-            float* dst = (float*)seg + (size_t)i * 256 + col0;
+            // columns 0..127 of X are B_p, 128..255 are M_p
+            float* dst = (float*)(seg + (col0 >= kTcD ? kSegM : kSegB)) + (size_t)i * kTcD + (col0 & (kTcD - 1));
 #pragma unroll
             for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
         }
@@ -1038,8 +1041,12 @@ __global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_rest(const __gr
 
 // Phase B: S_start(p+1) = M_p S_start(p) + B_p for p = 1 .. segs-2, from
 // S_start(1) (segment 0's end state), for one (sequence, head) and a
-// 16-column block of the state (columns of S are independent), fp32.
-__global__ void __launch_bounds__(256)
+// 16-column block of the state (columns of S are independent), fp32.  Each
+// M_p (64 KB) comes into shared memory with one bulk copy, two segments ahead
+// of its use; thread (r0, c) forms rows r0, r0 + 16, ... of column c.
+constexpr int kScanThreads = 256;
+constexpr uint32_t kScanSmem = 2 * 65536 + kTcD * 16 * 4 + 64 + 1024;
+__global__ void __launch_bounds__(kScanThreads, 1)
 kda_tc_scan_states(const int32_t* __restrict__ chunk_first, DeviceHeader* __restrict__ hdr, int H, int len0,
                    int len, uint8_t* __restrict__ segbuf, int segs_max) {
     if (hdr->status != KDA_OK) return;
@@ -1047,35 +1054,69 @@ kda_tc_scan_states(const int32_t* __restrict__ chunk_first, DeviceHeader* __rest
     const int nch = chunk_first[n + 1] - chunk_first[n];
     const int segs = seg_count(nch, len0, len);
     if (segs < 3) return;
-    __shared__ float S[kTcD][16];
-    const int tid = threadIdx.x, row = tid >> 1, half = (tid & 1) * 8;
-    const float* S1 = (const float*)(segbuf + ((size_t)nh * segs_max + 1) * kSegBytes + kSegMB);
-    for (int e = tid; e < kTcD * 16; e += 256) {
-        const int r = e >> 4, cc = e & 15;
-        S[r][cc] = S1[(size_t)r * kTcD + cblk + cc];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    float* Mbuf = (float*)sm;                               // [2][128][128]
+    float* S = (float*)(sm + 2 * 65536);                    // [128][16]
+    uint64_t* bar = (uint64_t*)(sm + 2 * 65536 + kTcD * 16 * 4);
+    const int tid = threadIdx.x, c = tid & 15, r0 = tid >> 4;
+    auto seg = [&](int p) { return segbuf + ((size_t)nh * segs_max + p) * kSegBytes; };
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
     }
     __syncthreads();
-    for (int p = 1; p + 1 < segs; ++p) {
-        const float* MB = (const float*)(segbuf + ((size_t)nh * segs_max + p) * kSegBytes);
-        const float* Mrow = MB + (size_t)row * 256 + kTcD;       // M_p row `row`
+    if (tid == 0) {
+        for (int p = 1; p <= 2 && p + 1 < segs; ++p) {
+            mbar_arrive_expect_tx(&bar[p - 1], 65536);
+            bulk_g2s(Mbuf + (p - 1) * kTcD * kTcD, seg(p) + kSegM, 65536, &bar[p - 1]);
+        }
+    }
+    const float* S1 = (const float*)(seg(1) + kSegMB);
+    for (int e = tid; e < kTcD * 16; e += kScanThreads) {
+        const int r = e >> 4, cc = e & 15;
+        S[e] = S1[(size_t)r * kTcD + cblk + cc];
+    }
+    __syncthreads();
+    bool good = true;
+    int p = 1;
+    for (; p + 1 < segs; ++p) {
+        const int b = (p - 1) & 1;
+        const float* Bp = (const float*)(seg(p) + kSegB);
         float acc[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = MB[(size_t)row * 256 + cblk + half + e];   // B_p
-        for (int kk = 0; kk < kTcD; kk += 4) {
-            const float4 m = *(const float4*)(Mrow + kk);
+        for (int j = 0; j < 8; ++j) acc[j] = Bp[(size_t)(r0 + 16 * j) * kTcD + cblk + c];
+        good = bar_and(kScanThreads, mbar_wait(&bar[b], ((p - 1) >> 1) & 1, kWaitNs));   // uniform
+        if (!good) break;
+        const float* M = Mbuf + b * kTcD * kTcD;
+        for (int k = 0; k < kTcD; k += 4) {
+            const float s0 = S[k * 16 + c], s1 = S[(k + 1) * 16 + c], s2 = S[(k + 2) * 16 + c],
+                        s3 = S[(k + 3) * 16 + c];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[e] += m.x * S[kk][half + e] + m.y * S[kk + 1][half + e] + m.z * S[kk + 2][half + e] +
-                          m.w * S[kk + 3][half + e];
+            for (int j = 0; j < 8; ++j) {
+                const float4 m = *(const float4*)(M + (r0 + 16 * j) * kTcD + k);
+                acc[j] = fmaf(m.x, s0, fmaf(m.y, s1, fmaf(m.z, s2, fmaf(m.w, s3, acc[j]))));
+            }
+        }
+        __syncthreads();                                     // S and this M buffer fully read
+        if (tid == 0 && p + 3 <= segs - 1) {                 // M_{p+2} into the buffer just read
+            mbar_arrive_expect_tx(&bar[b], 65536);
+            bulk_g2s(Mbuf + b * kTcD * kTcD, seg(p + 2) + kSegM, 65536, &bar[b]);
+        }
+        float* Snext = (float*)(seg(p + 1) + kSegMB);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = r0 + 16 * j;
+            S[r * 16 + c] = acc[j];
+            Snext[(size_t)r * kTcD + cblk + c] = acc[j];
         }
         __syncthreads();
-        float* Snext = (float*)(segbuf + ((size_t)nh * segs_max + p + 1) * kSegBytes + kSegMB);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            S[row][half + e] = acc[e];
-            Snext[(size_t)row * kTcD + cblk + half + e] = acc[e];
-        }
-        __syncthreads();
+    }
+    if (!good && tid == 0) {
+        record_status(hdr, KDA_ERR_TIMEOUT);
+        // the copies still in flight land before exit
+        for (int q = p; q <= p + 1 && q + 1 < segs; ++q) mbar_wait(&bar[(q - 1) & 1], ((q - 1) >> 1) & 1, kWaitNs);
     }
 }
 
@@ -1131,6 +1172,8 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
                                   (int)SmemC<256>::kBytes)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(kda_tc_chain_rest, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)SmemC<128>::kBytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kda_tc_scan_states, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kScanSmem)) != cudaSuccess) return e;
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[0], stream)) != cudaSuccess) return e;
     if (a.chunks_ub > 0 && T > 0) {
         CUtensorMap mv;
@@ -1156,7 +1199,7 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (plan.segs_max > 1) {
         if (plan.segs_max > 2) {
-            kda_tc_scan_states<<<dim3(nh, kTcD / 16), 256, 0, stream>>>(
+            kda_tc_scan_states<<<dim3(nh, kTcD / 16), kScanThreads, kScanSmem, stream>>>(
                 a.chunk_first, (DeviceHeader*)a.hdr, a.H, plan.len0, plan.len, ca.segbuf, plan.segs_max);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
