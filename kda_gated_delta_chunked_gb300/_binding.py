@@ -80,7 +80,7 @@ lib = _load()
 def prefill_kernel_files(dtype: str, d: int, flags: int = 0):
     """Source files of the two prefill kernels the library runs for a dtype and head size."""
     if dtype == "bf16" and d == 128 and not (flags & KDA_FLAG_CUDA_CORE_PREFILL):
-        files = ["kda_prefill_tc.cu", "kda_sm100.cuh", "kda_common.cuh"]
+        files = ["kda_prefill_tc.cu", "kda_tc_record.cuh", "kda_sm100.cuh", "kda_common.cuh"]
     else:
         files = ["kda_prefill_simt.cu", "kda_common.cuh"]
     return {"intra": files, "chain": files}
