@@ -78,8 +78,9 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
 /* kda_desc.flags bits. */
 enum {
-    /* Run the prefill on CUDA cores in fp32 even where the tensor-core path
-       applies (bf16, head size 128).  Slower; meant for cross-checking. */
+    /* Run the prefill (and kda_prefill_backward) on CUDA cores in fp32 even
+       where the tensor-core path applies (bf16, head size 128).  Slower; meant
+       for cross-checking. */
     KDA_FLAG_CUDA_CORE_PREFILL = 1,
     /* Scalar gate: log_alpha holds ONE value per (token, head) -- layout
        [T_tot, H] for the prefill, [N, H] for the decode step, aligned to its
@@ -192,10 +193,20 @@ KDA_API int kda_prefill_snapshots(const kda_desc *desc,
  *   d_initial_state  fp32 [N, H, d_k, d_v] or NULL (not written).
  * Gradients are 4-byte aligned, the states 16-byte aligned; no output may
  * overlap an input or another output.  desc->workspace must hold
- * kda_backward_workspace_bytes(desc) bytes: about 4 * H * d_k * d_v bytes
+ * kda_backward_workspace_bytes(desc) bytes (about 4 * H * d_k * d_v bytes
  * per 8 tokens of kept states plus 4 * (3 d_k + 1) * H * d_v / 32 bytes per
- * token of partial sums.  Runs on CUDA cores in fp32; results do not depend
- * on scheduling (no atomics).  Errors as for kda_prefill.
+ * token of partial sums, which also covers the tensor-core path's scratch).
+ *
+ * bf16 inputs with head size 128 run on the tensor cores: the forward is
+ * recomputed saving every 64-token chunk's end state, a reverse walk over the
+ * chunks gives each chunk's end-state gradient, and one kernel per (chunk,
+ * head) forms the gradients (bf16 operands, fp32 accumulation: gradients
+ * within about 1e-2 relative L2 of exact arithmetic).  A call in which some
+ * chunk's cumulative decay exceeds 2^100 in a channel (log alpha summed over
+ * the chunk below -69) runs instead on the fp32 CUDA-core path, decided on
+ * the device.  fp32 inputs, head size 64, or KDA_FLAG_CUDA_CORE_PREFILL take
+ * the fp32 CUDA-core path (about 1e-4).  Results do not depend on scheduling
+ * (no atomics).  Errors as for kda_prefill.
  */
 KDA_API size_t kda_backward_workspace_bytes(const kda_desc *desc);
 KDA_API int kda_prefill_backward(const kda_desc *desc,
