@@ -18,16 +18,20 @@
 // chunk, the recurrent state carried between chunks; the recurrence itself is
 // that of section 03.)
 //
-// Kernel (a), one CTA per (chunk, head), 256 threads, two CTAs per SM:
-//   1. Each thread owns 4 token rows x 8 key channels of the chunk: 16-byte
-//      loads of k, q, log_alpha (issued first thing, ahead of the set-up; a
-//      single sequence needs no table lookup for the chunk's bounds), a
-//      running sum of log alpha within its rows and a prefix over the 16 row
-//      groups through shared memory.  It then writes every scaled operand as
-//      bf16 with 16-byte stores, all token-major (no transposes): K~ = K 2^g,
+// Kernel (a), one CTA per (chunk, head), 256 threads, three CTAs per SM (80
+// registers, ~69 KB of shared memory, 128 TMEM columns each):
+//   1. Each thread owns 4 token rows x 8 key channels of the chunk: its 16-byte
+//      pieces of k, q, log_alpha are copied asynchronously (cp.async) into the
+//      shared-memory places the scaled operands will take, first thing, ahead
+//      of the set-up (a single sequence needs no table lookup for the chunk's
+//      bounds), so no register holds them; a sum of log alpha over its rows and
+//      a prefix over the 16 row groups through shared memory give each row's
+//      running sum.  It then writes every scaled operand as bf16 with 16-byte
+//      stores over the raw pieces, all token-major (no transposes): K~ = K 2^g,
 //      Q~ = Q 2^g, K^ = K 2^-g (g counted from the chunk start, in log2
 //      units), and K^end straight into the record.  V goes from HBM to the
-//      tensor core untouched (TMA, 128-byte swizzle).
+//      tensor core untouched (TMA, 128-byte swizzle), brought into L2 at the
+//      start and into shared memory after the solve, over the dead A^.
 //   2. MMA-a (M=128, N=64, K=128): [K~; Q~] K^^T gives the Gram block (rows
 //      0..63) and Q~ K^T (rows 64..127) in one TMEM accumulator.
 //   3. With A^[i][j] = beta_j (K~ K^T)[i][j] (j < i), the rows of
@@ -40,9 +44,9 @@
 //      recursion (one FMA per dependent step).  (Forming the diagonal-block
 //      inverses first, so that the sequential part is only the MMAs, was
 //      measured 1% slower: the recursion's work moves, it does not shrink.)
-//   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~ | V] with K~ read MN-major
-//      from the MMA-a operand (the [K~] half's K-steps issued as the solve
-//      stores each block of Y^); the epilogue forms Q' = Q~ - P T K~.  (A
+//   4. MMA-b (M=128, N=128 twice, K=64): Y^ [K~], then Y^ [V], each half in
+//      the same 128 TMEM columns, K~ read MN-major from the MMA-a operand; the
+//      first half's epilogue forms Q' = Q~ - P T K~.  (A
 //      reference point in mid-chunk, so that K~ and K^ stay within 2^+-50,
 //      needed a per-channel rescaling in the epilogue and was 5% slower.)
 //   5. The records kernel (b) reads are written as ready-to-copy shared-memory
@@ -120,23 +124,26 @@ __device__ __forceinline__ float bf_hi(uint32_t p) { return __uint_as_float(p & 
 // Kernel (a)
 // ---------------------------------------------------------------------------
 constexpr int kAThreads = 256;
-// TMEM columns: MMA-b's two halves at 0..127 ([K~]) and 128..255 ([V]); until
-// MMA-b's second half, the Gram / Q~ K^T block sits at 128..191 and the
-// coupling accumulators at 192..239.
-constexpr uint32_t kTmGram = 128;
-constexpr uint32_t kTmCpl = 192;
+// TMEM: 128 columns (three CTAs per SM).  Until the solve ends the Gram /
+// Q~ K^T block sits at columns 0..63 and the coupling accumulators at 64..111;
+// then MMA-b's two halves ([K~], then [V]) use columns 0..127 in turn.
+constexpr uint32_t kTmCols = 128;
+constexpr uint32_t kTmGram = 0;
+constexpr uint32_t kTmCpl = 64;
 
-struct SmemA {   // byte offsets from a 1024-aligned base; ~83 KB, two CTAs per SM
-    static constexpr uint32_t kV = 0;           // V tile (TMA, 128-byte swizzle), 2 x [64 tok x 64 ch]
-    static constexpr uint32_t kOpA = 16384;     // [K~; Q~], K-major 128B-swizzle, 2 K-blocks x 16 KB;
-                                                // MMA-a A, then MMA-b B (MN-major) and Q~ for the epilogue
-    static constexpr uint32_t kOpB1 = 49152;    // MMA-a B K^, K-major, 2 K-blocks x 8 KB; then:
-    static constexpr uint32_t kAt = 49152;      //   A^ by 16-column blocks, MN-major 32B-swizzle, 4 x 2 KB
-    static constexpr uint32_t kAt32 = 57344;    //   diagonal 16 x 16 blocks of A^, fp32 [64 rows][16], 4 KB
-    static constexpr uint32_t kY = 65536;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB
-    static constexpr uint32_t kPart = 65536;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
-    static constexpr uint32_t kGS = 49152;      // (slow path, before A^) g, fp32 [64][128], 32 KB
-    static constexpr uint32_t kMisc = 81920;    // beta[64], barriers, TMEM slot, flags, g_C, scalar gates[64]
+struct SmemA {   // byte offsets from a 1024-aligned base; ~69 KB, three CTAs per SM
+    static constexpr uint32_t kOpA = 0;         // [K~; Q~], K-major 128B-swizzle, 2 K-blocks x 16 KB;
+                                                // MMA-a A, then MMA-b B (MN-major), then the [W; Q'] image
+    static constexpr uint32_t kOpB1 = 32768;    // MMA-a B K^, K-major, 2 K-blocks x 8 KB; then:
+    static constexpr uint32_t kAt = 32768;      //   A^ by 16-column blocks, MN-major 32B-swizzle, 4 x 2 KB;
+                                                //   after the solve the V tile (TMA, 2 x [64 tok x 64 ch]),
+                                                //   then the U0 image
+    static constexpr uint32_t kV = 32768;
+    static constexpr uint32_t kAt32 = 40960;    //   diagonal 16 x 16 blocks of A^, fp32 [64 rows][16], 4 KB
+    static constexpr uint32_t kY = 49152;       // Y^ = [T; P T], bf16 K-major [128 x 64], 16 KB; then the O0 image
+    static constexpr uint32_t kPart = 49152;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
+    static constexpr uint32_t kGS = 32768;      // (slow path, before A^) g, fp32 [64][128], 32 KB
+    static constexpr uint32_t kMisc = 65536;    // beta[64], barriers, TMEM slot, flags, g_C, scalar gates[64]
     static constexpr uint32_t kBytes = kMisc + 2048 + 1024;
 };
 
@@ -183,9 +190,6 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
         for (int jt = J - 1; jt >= 0; --jt)
             mma_bf16_ss(tmem + kTmCpl + 16 * jt, ya,
                         sdesc(smem_u32(sm + SmemA::kAt + jt * 2048 + (J + 1) * 512), 2048, 256, 6), id, J + 1 < 3);
-        // K-step J+1 of MMA-b's first half, Y^ [K~], into columns 0..127.
-        mma_bf16_ss(tmem, ya, sdesc(smem_u32(sm + SmemA::kOpA + (J + 1) * 2048), 16384, 1024, 2),
-                    idesc_bf16(128, 128, 0, 1), J + 1 < 3);
     }
     if (warp < 4) {
         float z[16];
@@ -239,7 +243,7 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
 }
 
 template <bool kScalarGate>
-__global__ void __launch_bounds__(kAThreads, 2)
+__global__ void __launch_bounds__(kAThreads, 3)
 kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ q,
                    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ log_alpha,
                    const __nv_bfloat16* __restrict__ beta, const int32_t* __restrict__ cu,
@@ -280,26 +284,28 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         len = (int)min64(kChunk, seq_end - t0);
     }
 
-    // ---- pass A: thread owns rows 4R..4R+3, channels 8C..8C+7.  The 16-byte
-    // loads of k, q, log alpha (and beta) are issued first, before the status
-    // check and the set-up below, so their latency overlaps both (volatile:
-    // the compiler keeps them ahead of the status branch).
+    // ---- pass A: thread owns rows 4R..4R+3, channels 8C..8C+7.  Its 16-byte
+    // pieces of k, q and log alpha are copied asynchronously into shared
+    // memory first thing, straight into the places where the scaled operands
+    // will be written over them (k, q in [K~; Q~], log alpha in K^), so no
+    // register holds them meanwhile; rows past the chunk are zero-filled.
     const int R = tid >> 4, C = tid & 15;
     const size_t rs = (size_t)H * kTcD;                       // elements between tokens
     const size_t base = ((size_t)t0 * H + h) * kTcD + 8 * C;
-    uint4 kr[4], qr[4], lr[4];
-    uint32_t braw = 0, lraw = 0;
+    const uint32_t kbA = (uint32_t)C >> 3, ccA = (uint32_t)(C & 7) * 8u;
+    {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = 4 * R + i;
-        const size_t gi = base + (size_t)r * rs;
-        kr[i] = qr[i] = lr[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < len) {
-            kr[i] = ld_nc_v4(k + gi);
-            qr[i] = ld_nc_v4(q + gi);
-            if (!kScalarGate) lr[i] = ld_nc_v4(log_alpha + gi);
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * R + i;
+            const uint32_t nb = r < len ? 16u : 0u;
+            const size_t gi = base + (size_t)(r < len ? r : 0) * rs;
+            cp_async16(sm + SmemA::kOpA + kbA * 16384 + sw128_off(r, ccA), k + gi, nb);
+            cp_async16(sm + SmemA::kOpA + kbA * 16384 + sw128_off(64 + r, ccA), q + gi, nb);
+            if (!kScalarGate) cp_async16(sm + SmemA::kOpB1 + kbA * 8192 + sw128_off(r, ccA), log_alpha + gi, nb);
         }
+        cp_async_commit();
     }
+    uint32_t braw = 0, lraw = 0;
     // beta, and with the scalar gate the chunk's 64 gates, one per thread
     // (loaded once and shared: 4 scalar loads per thread were 10% slower).
     if (tid < len) {
@@ -319,30 +325,33 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     }
     if (kScalarGate && tid < kChunk) s_lg[tid] = __uint_as_float(lraw << 16);
     __syncthreads();
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[0], 16384);
-        tma_load_3d(sm + SmemA::kV, &tm_v, 0, h, (int)t0, &bars[0]);
-        tma_load_3d(sm + SmemA::kV + 8192, &tm_v, 64, h, (int)t0, &bars[0]);
+    if (tid == 0) {                    // V is loaded after the solve; bring it into L2 now
+        tma_prefetch_3d(&tm_v, 0, h, (int)t0);
+        tma_prefetch_3d(&tm_v, 64, h, (int)t0);
     }
     if (tid < kChunk) s_beta[tid] = __uint_as_float(braw << 16);
-    if (warp == 0) { tmem_alloc(s_tmem, 256); tmem_relinquish(); }
+    if (warp == 0) { tmem_alloc(s_tmem, kTmCols); tmem_relinquish(); }
 
-    // Running sum of log alpha (log2 units) within the thread's 4 rows.
-    float gl[4][8];
+    // Sum of log alpha (log2 units) over the thread's 4 rows; pass B forms the
+    // running sums again row by row (they would hold 32 registers meanwhile).
+    cp_async_wait_all();
+    auto la_row = [&](int i, float (&la)[8]) {
+        if (kScalarGate) {
+            const float l = s_lg[4 * R + i];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) la[e] = l;
+        } else {
+            unpack8(*(const uint4*)(sm + SmemA::kOpB1 + kbA * 8192 + sw128_off(4 * R + i, ccA)), la);
+        }
+    };
     {
         float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float la[8];
-            if (kScalarGate) {
-                const float l = s_lg[4 * R + i];
+            la_row(i, la);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) la[e] = l;
-            } else {
-                unpack8(lr[i], la);
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { s8[e] = fmaf(la[e], kLog2e, s8[e]); gl[i][e] = s8[e]; }
+            for (int e = 0; e < 8; ++e) s8[e] = fmaf(la[e], kLog2e, s8[e]);
         }
         float4* part = (float4*)(sm + SmemA::kPart) + (R * kTcD + 8 * C) / 4;
         part[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
@@ -379,11 +388,12 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     }
     const uint32_t tmem = *s_tmem;
     if (status != KDA_OK) {            // uniform; nothing has been written yet
-        if (warp == 0) tmem_dealloc(tmem, 256);
-        if (tid == 0) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
+        if (warp == 0) tmem_dealloc(tmem, kTmCols);
         return;
     }
     const bool slow = s_flag[0] != 0;
+    // The slow path's g scratch overlaps the prefix sums just read: all reads first.
+    if (slow) __syncthreads();
     if (slow && tid == 0) hdr->pad[kHdrSlowChunk] = 1;   // some chunk needs the slow path
     if (R == 0) {
 #pragma unroll
@@ -396,42 +406,75 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         uint8_t* opA = sm + SmemA::kOpA + kb * 16384;
         uint8_t* opB1 = sm + SmemA::kOpB1 + kb * 8192;
         uint8_t* ke = rec + TcRec::kKE + kb * 8192;
-        float* gS = (float*)(sm + SmemA::kGS);
-        // On the fast path -g_C <= 100 and g_r lies in [g_C, 0] (log alpha <= 0),
-        // so every exponent below is within [-100, 100].
-        float fC[8];
+        float gr[8];                                       // running g_r (log2 units)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) fC[e] = slow ? 0.f : ex2_fast(gC[e]);
+        for (int e = 0; e < 8; ++e) gr[e] = gbase[e];
+        if (!slow) {
+            // -g_C <= 100 and g_r lies in [g_C, 0] (log alpha <= 0), so every
+            // exponent below is within [-100, 100].
+            float fC[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 4 * R + i;
-            float kv[8], qv[8], km[8], qm[8], kh[8], kend[8];
-            unpack8(kr[i], kv);
-            unpack8(qr[i], qv);
+            for (int e = 0; e < 8; ++e) fC[e] = ex2_fast(gC[e]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (!slow) {
-                    const float dr = gl[i][e] + gbase[e];      // g_r
-                    const float e1 = ex2_fast(dr);             // 2^g_r
-                    const float e2 = ex2_fast(-dr);            // 2^-g_r
+            for (int i = 0; i < 4; ++i) {
+                const int r = 4 * R + i;
+                {
+                    float la[8];
+                    la_row(i, la);                         // read before K^ is written over it
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gr[e] = fmaf(la[e], kLog2e, gr[e]);
+                }
+                float kv[8], qv[8], km[8], qm[8], kh[8], kend[8];
+                const uint32_t off = sw128_off(r, cc), offq = sw128_off(64 + r, cc);
+                unpack8(*(const uint4*)(opA + off), kv);
+                unpack8(*(const uint4*)(opA + offq), qv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float e1 = ex2_fast(gr[e]);      // 2^g_r
+                    const float e2 = ex2_fast(-gr[e]);     // 2^-g_r
                     km[e] = kv[e] * e1;
                     qm[e] = qv[e] * e1;
                     kh[e] = kv[e] * e2;
-                    kend[e] = kh[e] * fC[e];                   // k 2^(g_C - g_r) <= |k|
-                } else {
-                    const float g = gbase[e] + gl[i][e];
+                    kend[e] = kh[e] * fC[e];               // k 2^(g_C - g_r) <= |k|
+                }
+                *(uint4*)(opA + off) = pack8(km);
+                *(uint4*)(opA + offq) = pack8(qm);
+                *(uint4*)(opB1 + off) = pack8(kh);
+                *(uint4*)(ke + off) = pack8(kend);
+            }
+        } else {
+            // The slow path's fp32 g scratch overlays log alpha: every thread
+            // reads its four rows before any of it is written.
+            float gl[4][8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float la[8];
+                la_row(i, la);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { gr[e] = fmaf(la[e], kLog2e, gr[e]); gl[i][e] = gr[e]; }
+            }
+            __syncthreads();
+            float* gS = (float*)(sm + SmemA::kGS);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 4 * R + i;
+                float kv[8], qv[8], km[8], qm[8], kend[8];
+                const uint32_t off = sw128_off(r, cc), offq = sw128_off(64 + r, cc);
+                unpack8(*(const uint4*)(opA + off), kv);
+                unpack8(*(const uint4*)(opA + offq), qv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float g = gl[i][e];
                     const float e3 = exp2f(g);
                     km[e] = kv[e] * e3;
                     qm[e] = qv[e] * e3;
                     kend[e] = kv[e] * exp2f(gC[e] - g);
                     gS[r * kTcD + 8 * C + e] = g;
                 }
+                *(uint4*)(opA + off) = pack8(km);
+                *(uint4*)(opA + offq) = pack8(qm);
+                *(uint4*)(ke + off) = pack8(kend);
             }
-            const uint32_t off = sw128_off(r, cc);
-            *(uint4*)(opA + off) = pack8(km);
-            *(uint4*)(opA + sw128_off(64 + r, cc)) = pack8(qm);
-            if (!slow) *(uint4*)(opB1 + off) = pack8(kh);
-            *(uint4*)(ke + off) = pack8(kend);
         }
     }
     fence_proxy_async_smem();
@@ -439,6 +482,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
 
     uint32_t mph = 0;                 // completed phases of bars[1]
     bool abort = false;
+    bool v_issued = false;            // (thread 0) the V tile copy is in flight
     if (!slow) {
         if (tid == 0) {
             const uint32_t id = idesc_bf16(128, 64);
@@ -527,36 +571,34 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     inv_block<1>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
     inv_block<0>(sm, tmem, s_beta, &bars[1], s_flag, mph, abort);
 
-    // ---- MMA-b: Y^ [K~ | V] -> [[W, U0], [P T K~, O0]].  K-steps 3..1
-    // of the [K~] half were issued during the solve, as each block of Y^ was
-    // stored; here the last one and the [V] half, whose issuing thread waits
-    // for the V tile first (the MMA reads it).
-    if (tid == 0 && !abort && !mbar_wait(&bars[0], 0, kWaitNs)) { s_flag[1] = 1; abort = true; }
+    // ---- MMA-b, first half: Y^ [K~] -> [W; P T K~] in columns 0..127 (the Gram
+    // and coupling accumulators are dead).  V is loaded into the dead A^ region.
     if (tid == 0 && !abort) {
+        mbar_arrive_expect_tx(&bars[0], 16384);
+        tma_load_3d(sm + SmemA::kV, &tm_v, 0, h, (int)t0, &bars[0]);
+        tma_load_3d(sm + SmemA::kV + 8192, &tm_v, 64, h, (int)t0, &bars[0]);
+        v_issued = true;
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
-        mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kY)),
-                    sdesc(smem_u32(sm + SmemA::kOpA), 16384, 1024, 2), id, true);   // last K-step of the [K~] half
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(tmem + 128, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
-                        sdesc(smem_u32(sm + SmemA::kV + ks * 2048), 8192, 1024, 2), id, ks > 0);
+            mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
+                        sdesc(smem_u32(sm + SmemA::kOpA + ks * 2048), 16384, 1024, 2), id, ks > 0);
         mma_commit(&bars[1]);
     }
-    __syncthreads();
-    abort = s_flag[1] != 0;
     if (!abort && !mbar_wait(&bars[1], mph & 1, kWaitNs)) s_flag[1] = 1;
     ++mph;
     tc_fence_after_sync();
     __syncthreads();
     abort = s_flag[1] != 0;
 
-    // ---- epilogue.  Lane quarters 0,1: rows 0..63 = [W | U0]; quarters 2,3:
-    // rows 64..127 = [P T K~ | O0].  The two warps of a quarter split columns.
+    // ---- epilogue, first half.  Lane quarters 0,1: rows 0..63 = W; quarters
+    // 2,3: rows 64..127 = P T K~ -> Q' = Q~ - P T K~.  The two warps of a quarter
+    // split the columns; the [W; Q'] image is staged in place over [K~; Q~].
+    const int quarter = warp & 3, half = warp >> 2;
+    const int i = (quarter & 1) * 32 + lane;      // token row within the chunk
+    const bool top = quarter < 2;
     if (!abort) {
-        const int quarter = warp & 3, half = warp >> 2;
-        const int i = (quarter & 1) * 32 + lane;      // token row within the chunk
-        const bool top = quarter < 2;
-        uint8_t* a1 = sm + SmemA::kOpA;               // [W; Q'] image, in place over [K~; Q~]
+        uint8_t* a1 = sm + SmemA::kOpA;
         const uint8_t* qm = sm + SmemA::kOpA;
 #pragma unroll 1
         for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
@@ -578,11 +620,38 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin)) = pack8(lo);
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = pack8(hi);
         }
+    }
+    tc_fence_before_sync();
+    __syncthreads();                   // the first half's accumulator has been read
+    tc_fence_after_sync();
+
+    // ---- MMA-b, second half: Y^ [V] -> [U0; O0] in columns 0..127; the issuing
+    // thread waits for the V tile first.
+    if (tid == 0 && !abort && !mbar_wait(&bars[0], 0, kWaitNs)) { s_flag[1] = 1; abort = true; }
+    if (tid == 0 && !abort) {
+        const uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
+                        sdesc(smem_u32(sm + SmemA::kV + ks * 2048), 8192, 1024, 2), id, ks > 0);
+        mma_commit(&bars[1]);
+    }
+    __syncthreads();
+    abort = s_flag[1] != 0;
+    if (!abort && !mbar_wait(&bars[1], mph & 1, kWaitNs)) s_flag[1] = 1;
+    ++mph;
+    tc_fence_after_sync();
+    __syncthreads();
+    abort = s_flag[1] != 0;
+
+    // ---- epilogue, second half: U0 (rows 0..63) and O0 (rows 64..127) images in
+    // 16-column tiles over the dead V tile and Y^.
+    if (!abort) {
         uint8_t* uo = sm + SmemA::kAt + (top ? 0 : TcRec::kO0 - TcRec::kU0);   // U0 | O0 images
 #pragma unroll 1
         for (int t = 4 * half; t < 4 * half + 4; ++t) {
             float f[16];
-            tmem_ld16(tmem_addr(tmem, 32 * quarter, 128 + t * kTile), f);
+            tmem_ld16(tmem_addr(tmem, 32 * quarter, t * kTile), f);
             tmem_wait_ld();
             float lo[8], hi[8];
 #pragma unroll
@@ -596,7 +665,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, kTmCols);
     if (!abort) {                      // coalesced copy of the staged images to the record
         static_assert(SmemA::kAt + 2 * (TcRec::kO0 - TcRec::kU0) <= SmemA::kMisc, "staging fits");
 #pragma unroll 4
@@ -606,7 +675,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             *(uint4*)(rec + (e < 2048 ? TcRec::kA1 : TcRec::kU0) + off) = x;
         }
     }
-    if (tid == 0) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
+    if (tid == 0 && v_issued) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
 }
 
 // ---------------------------------------------------------------------------

@@ -83,6 +83,15 @@ __device__ __forceinline__ bool bar_and_id(uint32_t id, uint32_t nthreads, bool 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// 16-byte asynchronous copy global -> shared by one thread (L2 only); src_bytes
+// < 16 zero-fills the rest (0: nothing is read).  Completed by cp_async_wait_all
+// in the same thread.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
 // dst, src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -122,6 +131,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         " [%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
           "r"(smem_u32(bar)) : "memory");
+}
+// Hint: bring the box of a 3-D tensor map at (x, y, z) into L2.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z) : "memory");
 }
 // 3-D tiled tensor store (TMA) from shared memory, in the thread's bulk async-group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
