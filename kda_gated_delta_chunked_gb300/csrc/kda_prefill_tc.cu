@@ -663,19 +663,21 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     } else if (tid == 0) {
         record_status(hdr, KDA_ERR_TIMEOUT);
     }
+    fence_proxy_async_smem();          // the staged images are visible to the bulk copy engine
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmCols);
-    if (!abort) {                      // coalesced copy of the staged images to the record
-        static_assert(SmemA::kAt + 2 * (TcRec::kO0 - TcRec::kU0) <= SmemA::kMisc, "staging fits");
-#pragma unroll 4
-        for (int e = tid; e < 4096; e += kAThreads) {
-            const uint32_t off = e < 2048 ? (uint32_t)e * 16u : (uint32_t)(e - 2048) * 16u;
-            const uint4 x = *(const uint4*)(sm + (e < 2048 ? SmemA::kOpA : SmemA::kAt) + off);
-            *(uint4*)(rec + (e < 2048 ? TcRec::kA1 : TcRec::kU0) + off) = x;
+    if (tid == 0) {
+        if (!abort) {                  // the [W; Q'] and [U0; O0] images go to the record in two bulk stores
+            static_assert(SmemA::kAt + 2 * (TcRec::kO0 - TcRec::kU0) <= SmemA::kMisc, "staging fits");
+            static_assert(TcRec::kU0 - TcRec::kA1 >= 32768 && TcRec::kO0 + 16384 <= TcRec::kGam, "record spans");
+            bulk_s2g(rec + TcRec::kA1, sm + SmemA::kOpA, 32768);
+            bulk_s2g(rec + TcRec::kU0, sm + SmemA::kAt, 32768);
+            bulk_commit();
+            bulk_wait_read_all();      // shared memory stays valid until the engine has read it
         }
+        if (v_issued) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
     }
-    if (tid == 0 && v_issued) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
 }
 
 // ---------------------------------------------------------------------------
