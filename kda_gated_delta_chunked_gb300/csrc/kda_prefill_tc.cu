@@ -20,18 +20,21 @@
 //
 // Kernel (a), one CTA per (chunk, head), 256 threads, three CTAs per SM (80
 // registers, ~69 KB of shared memory, 128 TMEM columns each):
-//   1. Each thread owns 4 token rows x 8 key channels of the chunk: its 16-byte
-//      pieces of k, q, log_alpha are copied asynchronously (cp.async) into the
-//      shared-memory places the scaled operands will take, first thing, ahead
-//      of the set-up (a single sequence needs no table lookup for the chunk's
-//      bounds), so no register holds them; a sum of log alpha over its rows and
-//      a prefix over the 16 row groups through shared memory give each row's
-//      running sum.  It then writes every scaled operand as bf16 with 16-byte
-//      stores over the raw pieces, all token-major (no transposes): K~ = K 2^g,
-//      Q~ = Q 2^g, K^ = K 2^-g (g counted from the chunk start, in log2
-//      units), and K^end straight into the record.  V goes from HBM to the
-//      tensor core untouched (TMA, 128-byte swizzle), brought into L2 at the
-//      start and into shared memory after the solve, over the dead A^.
+//   1. One thread starts TMA copies of k, q (and log alpha) into the
+//      shared-memory places the scaled operands will take (128-byte swizzle,
+//      64 tokens x 64 channels a box), first thing, ahead of the set-up (a
+//      single sequence needs no table lookup for the chunk's bounds); rows past
+//      the sequence end are zeroed after the copy lands.  (Per-thread 16-byte
+//      cp.async pieces instead were 3% slower.)  Each thread owns 4 token rows
+//      x 8 key channels: a sum of log alpha over its rows and a prefix over the
+//      16 row groups through shared memory give each row's running sum.  It then
+//      writes every scaled operand as bf16 with 16-byte stores over the raw
+//      pieces, all token-major (no transposes): K~ = K 2^g, Q~ = Q 2^g,
+//      K^ = K 2^-g (g counted from the chunk start, in log2 units), and K^end
+//      straight into the record.  V goes from HBM to the tensor core untouched
+//      (TMA, 128-byte swizzle), brought into L2 at the start and into shared
+//      memory after the solve, over the dead A^ (loading half of it at the
+//      start into 8 KB more shared memory was 1% slower).
 //   2. MMA-a (M=128, N=64, K=128): [K~; Q~] K^^T gives the Gram block (rows
 //      0..63) and Q~ K^T (rows 64..127) in one TMEM accumulator.
 //   3. With A^[i][j] = beta_j (K~ K^T)[i][j] (j < i), the rows of
@@ -52,9 +55,10 @@
 //   5. The records kernel (b) reads are written as ready-to-copy shared-memory
 //      images: [W; Q'] (K-major, 128-byte swizzle), K^end (token-major), U0 /
 //      O0 in 16-column tiles, Gamma.  [W; Q'] and U0 / O0 are staged in shared
-//      memory (in place over the dead operands) and copied out with coalesced
-//      16-byte stores: written straight from the accumulator rows, every lane
-//      of a store touched its own 128-byte line (9% slower).
+//      memory (in place over the dead operands) and leave in 1-D bulk stores,
+//      [W; Q'] while the second half of MMA-b runs.  (A coalesced 16-byte copy
+//      by all threads was 4% slower, and stores straight from the accumulator
+//      rows, where every lane of a store touched its own 128-byte line, 9%.)
 // Chunks whose cumulative decay from the chunk start exceeds 2^100 in some
 // channel cannot use this factorisation (K^ would leave the range where the
 // products stay finite in fp32); for those the Gram and Q~ K^T rows are formed
@@ -144,7 +148,7 @@ struct SmemA {   // byte offsets from a 1024-aligned base; ~69 KB, three CTAs pe
     static constexpr uint32_t kPart = 49152;    // (before Y^) per-row-group sums of log alpha, fp32 [16][128]
     static constexpr uint32_t kGS = 32768;      // (slow path, before A^) g, fp32 [64][128], 32 KB
     static constexpr uint32_t kMisc = 65536;    // beta[64], barriers, TMEM slot, flags, g_C, scalar gates[64]
-    static constexpr uint32_t kBytes = kMisc + 2048 + 1024;
+    static constexpr uint32_t kBytes = kMisc + 2304 + 1024;   // misc ends at +2304; 1024 to align the base
 };
 
 // Byte offset of (row m, column n < 16) in a 16-column block of an MN-major
@@ -244,7 +248,10 @@ __device__ __forceinline__ void inv_block(uint8_t* sm, uint32_t tmem, const floa
 
 template <bool kScalarGate>
 __global__ void __launch_bounds__(kAThreads, 3)
-kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ q,
+kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_la,
+                   const __nv_bfloat16* __restrict__ q,
                    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ log_alpha,
                    const __nv_bfloat16* __restrict__ beta, const int32_t* __restrict__ cu,
                    DeviceHeader* __restrict__ hdr, const int32_t* __restrict__ chunk_first, int N, int H,
@@ -252,7 +259,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* s_beta = (float*)(sm + SmemA::kMisc);                 // [64]
-    uint64_t* bars = (uint64_t*)(sm + SmemA::kMisc + 768);       // [0] V tile, [1] MMAs
+    uint64_t* bars = (uint64_t*)(sm + SmemA::kMisc + 768);       // [0] V tile, [1] MMAs, [2] inputs
     uint32_t* s_tmem = (uint32_t*)(sm + SmemA::kMisc + 800);
     int* s_flag = (int*)(sm + SmemA::kMisc + 816);                // [0] slow path, [1] abort
     float* s_gtot = (float*)(sm + SmemA::kMisc + 1024);           // [128] g_C per channel
@@ -284,26 +291,24 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         len = (int)min64(kChunk, seq_end - t0);
     }
 
-    // ---- pass A: thread owns rows 4R..4R+3, channels 8C..8C+7.  Its 16-byte
-    // pieces of k, q and log alpha are copied asynchronously into shared
-    // memory first thing, straight into the places where the scaled operands
-    // will be written over them (k, q in [K~; Q~], log alpha in K^), so no
-    // register holds them meanwhile; rows past the chunk are zero-filled.
-    const int R = tid >> 4, C = tid & 15;
-    const size_t rs = (size_t)H * kTcD;                       // elements between tokens
-    const size_t base = ((size_t)t0 * H + h) * kTcD + 8 * C;
-    const uint32_t kbA = (uint32_t)C >> 3, ccA = (uint32_t)(C & 7) * 8u;
-    {
+    // ---- inputs: k and q are copied by TMA into [K~; Q~] and log alpha into
+    // K^ (64 tokens x 64 channels a box, 128-byte swizzle), the places where
+    // the scaled operands are written over them, so no register holds them
+    // meanwhile; rows past the sequence are zeroed once the copy has landed.
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
+        fence_mbar_init();
+        s_flag[0] = 0;
+        s_flag[1] = 0;
+        mbar_arrive_expect_tx(&bars[2], kScalarGate ? 32768 : 49152);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 4 * R + i;
-            const uint32_t nb = r < len ? 16u : 0u;
-            const size_t gi = base + (size_t)(r < len ? r : 0) * rs;
-            cp_async16(sm + SmemA::kOpA + kbA * 16384 + sw128_off(r, ccA), k + gi, nb);
-            cp_async16(sm + SmemA::kOpA + kbA * 16384 + sw128_off(64 + r, ccA), q + gi, nb);
-            if (!kScalarGate) cp_async16(sm + SmemA::kOpB1 + kbA * 8192 + sw128_off(r, ccA), log_alpha + gi, nb);
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_3d(sm + SmemA::kOpA + kb * 16384, &tm_k, 64 * kb, h, (int)t0, &bars[2]);
+            tma_load_3d(sm + SmemA::kOpA + kb * 16384 + 8192, &tm_q, 64 * kb, h, (int)t0, &bars[2]);
+            if (!kScalarGate) tma_load_3d(sm + SmemA::kOpB1 + kb * 8192, &tm_la, 64 * kb, h, (int)t0, &bars[2]);
         }
-        cp_async_commit();
     }
     uint32_t braw = 0, lraw = 0;
     // beta, and with the scalar gate the chunk's 64 gates, one per thread
@@ -315,14 +320,6 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     // (a single sequence checks the status word after the prefix below, before
     // its first write, so the set-up does not wait for it)
     uint8_t* rec = recs + ((size_t)c * H + h) * TcRec::kBytes;
-
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        fence_mbar_init();
-        s_flag[0] = 0;
-        s_flag[1] = 0;
-    }
     if (kScalarGate && tid < kChunk) s_lg[tid] = __uint_as_float(lraw << 16);
     __syncthreads();
     if (tid == 0) {                    // V is loaded after the solve; bring it into L2 now
@@ -332,9 +329,25 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     if (tid < kChunk) s_beta[tid] = __uint_as_float(braw << 16);
     if (warp == 0) { tmem_alloc(s_tmem, kTmCols); tmem_relinquish(); }
 
-    // Sum of log alpha (log2 units) over the thread's 4 rows; pass B forms the
-    // running sums again row by row (they would hold 32 registers meanwhile).
-    cp_async_wait_all();
+    // ---- pass A: thread owns rows 4R..4R+3, channels 8C..8C+7: the sum of log
+    // alpha (log2 units) over its rows; pass B forms the running sums again row
+    // by row (they would hold 32 registers meanwhile).
+    const int R = tid >> 4, C = tid & 15;
+    const uint32_t kbA = (uint32_t)C >> 3, ccA = (uint32_t)(C & 7) * 8u;
+    bool in_late = false;              // the input copy outlived the wait (error path)
+    if (!mbar_wait(&bars[2], 0, kWaitNs)) { s_flag[1] = 1; in_late = true; }
+    if (len < kChunk) {                // rows past the sequence hold the next one's tokens: zero them
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * R + i;
+            if (r >= len) {
+                *(uint4*)(sm + SmemA::kOpA + kbA * 16384 + sw128_off(r, ccA)) = make_uint4(0, 0, 0, 0);
+                *(uint4*)(sm + SmemA::kOpA + kbA * 16384 + sw128_off(64 + r, ccA)) = make_uint4(0, 0, 0, 0);
+                if (!kScalarGate)
+                    *(uint4*)(sm + SmemA::kOpB1 + kbA * 8192 + sw128_off(r, ccA)) = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
     auto la_row = [&](int i, float (&la)[8]) {
         if (kScalarGate) {
             const float l = s_lg[4 * R + i];
@@ -389,6 +402,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
     const uint32_t tmem = *s_tmem;
     if (status != KDA_OK) {            // uniform; nothing has been written yet
         if (warp == 0) tmem_dealloc(tmem, kTmCols);
+        if (in_late) mbar_wait(&bars[2], 0, kWaitNs);
         return;
     }
     const bool slow = s_flag[0] != 0;
@@ -621,6 +635,7 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             *(uint4*)(a1 + kb * 16384 + sw128_off(row, kin + 8)) = pack8(hi);
         }
     }
+    fence_proxy_async_smem();          // the [W; Q'] image is visible to the bulk copy engine
     tc_fence_before_sync();
     __syncthreads();                   // the first half's accumulator has been read
     tc_fence_after_sync();
@@ -635,6 +650,8 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
             mma_bf16_ss(tmem, sdesc_k_sw128(smem_u32(sm + SmemA::kY + ks * 32)),
                         sdesc(smem_u32(sm + SmemA::kV + ks * 2048), 8192, 1024, 2), id, ks > 0);
         mma_commit(&bars[1]);
+        bulk_s2g(rec + TcRec::kA1, sm + SmemA::kOpA, 32768);
+        bulk_commit();
     }
     __syncthreads();
     abort = s_flag[1] != 0;
@@ -671,12 +688,12 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16
         if (!abort) {                  // the [W; Q'] and [U0; O0] images go to the record in two bulk stores
             static_assert(SmemA::kAt + 2 * (TcRec::kO0 - TcRec::kU0) <= SmemA::kMisc, "staging fits");
             static_assert(TcRec::kU0 - TcRec::kA1 >= 32768 && TcRec::kO0 + 16384 <= TcRec::kGam, "record spans");
-            bulk_s2g(rec + TcRec::kA1, sm + SmemA::kOpA, 32768);
             bulk_s2g(rec + TcRec::kU0, sm + SmemA::kAt, 32768);
             bulk_commit();
-            bulk_wait_read_all();      // shared memory stays valid until the engine has read it
         }
+        bulk_wait_read_all();          // shared memory stays valid until the engine has read it
         if (v_issued) mbar_wait(&bars[0], 0, kWaitNs);   // the V tile copy has landed before exit
+        if (in_late) mbar_wait(&bars[2], 0, kWaitNs);
     }
 }
 
@@ -1206,8 +1223,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// V [T, H, 128] bf16; box = 64 tokens x 64 channels of one head, 128-byte
-// swizzle (the MN-major operand layout of the second intra-chunk product).
+// k, q, log alpha, V [T, H, 128] bf16; box = 64 tokens x 64 channels of one
+// head, 128-byte swizzle (the K-major operand layout of the first intra-chunk
+// product for k and q, the MN-major one of the second for V).
 // out [T, H, 128] bf16; box = 16 channels x 1 head x 64 tokens, no swizzle
 // (the layout of a U0 / O0 record tile).
 static bool make_out_map(CUtensorMap* m, void* base, int64_t T, int H) {
@@ -1249,8 +1267,14 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
     if (a.chunks_ub > 0 && T > 0) {
         CUtensorMap mv;
         if (!make_v_map(&mv, a.v, T, a.H)) return cudaErrorInvalidValue;
+        CUtensorMap mk, mq, ml;
+        if (!make_v_map(&mk, a.k, T, a.H) || !make_v_map(&mq, a.q, T, a.H)) return cudaErrorInvalidValue;
+        if (a.la_scalar) ml = mk;
+        else if (!make_v_map(&ml, a.la, T, a.H)) return cudaErrorInvalidValue;
         intra<<<dim3(a.chunks_ub, a.H), kAThreads, SmemA::kBytes, stream>>>(
-            mv, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.la,
+            mv,
+            mk, mq, ml,
+            (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.la,
             (const __nv_bfloat16*)a.beta, a.cu, (DeviceHeader*)a.hdr, a.chunk_first, a.N, a.H, T, (uint8_t*)a.recs);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
