@@ -75,7 +75,10 @@
 //   MMA3 (M=128, N=128, K=64):  K^end^T U  -> S <- Gamma * S + K^end^T U
 // with S and U fed back to the tensor core as bf16 MN-major operands.  Long
 // sequences are cut into segments that run in parallel (see the segment scan
-// below the kernel (a) code).
+// below the kernel (a) code); the transition passes that map each segment's
+// start state to its end state take the step as one product, S <- Diag(Gamma)
+// S + N S + [B | 0] with N = -K^end^T W and B = K^end^T U0 formed a chunk ahead,
+// and have an MMA-issuing warp of their own.
 //
 // Every wait on an mbarrier is bounded; on timeout the kernel records
 // KDA_ERR_TIMEOUT in the device status word, drains its own copies and exits.
@@ -661,8 +664,9 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v,
     __syncthreads();
     abort = s_flag[1] != 0;
 
-    // ---- epilogue, second half: U0 (rows 0..63) and O0 (rows 64..127) images in
-    // 16-column tiles over the dead V tile and Y^.
+    // ---- epilogue, second half: the U0 image (rows 0..63; token-major, two
+    // 64-channel blocks in 128-byte swizzle, an MN-major operand of the chain)
+    // and the O0 image (rows 64..127; 16-column tiles) over the dead V tile and Y^.
     if (!abort) {
         uint8_t* uo = sm + SmemA::kAt + (top ? 0 : TcRec::kO0 - TcRec::kU0);   // U0 | O0 images
 #pragma unroll 1
@@ -673,9 +677,16 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v,
             float lo[8], hi[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) { lo[e] = f[e]; hi[e] = f[8 + e]; }
-            uint4* dst = (uint4*)(uo + t * TcRec::kTileBytes + i * (kTile * 2));
-            dst[0] = pack8(lo);
-            dst[1] = pack8(hi);
+            if (top) {
+                const uint32_t c = (uint32_t)t * kTile;
+                uint8_t* ub = uo + (c >> 6) * 8192u;
+                *(uint4*)(ub + sw128_off(i, c & 63u)) = pack8(lo);
+                *(uint4*)(ub + sw128_off(i, (c & 63u) + 8u)) = pack8(hi);
+            } else {
+                uint4* dst = (uint4*)(uo + t * TcRec::kTileBytes + i * (kTile * 2));
+                dst[0] = pack8(lo);
+                dst[1] = pack8(hi);
+            }
         }
     } else if (tid == 0) {
         record_status(hdr, KDA_ERR_TIMEOUT);
@@ -704,20 +715,21 @@ kda_tc_intra_chunk(const __grid_constant__ CUtensorMap tm_v,
 // Segment 0 is [0, L0) and segment p >= 1 is [L0 + (p-1) L, L0 + p L):
 //   launch 1: segment 0 runs the output pass (OUT, N = 128) from the initial
 //      state, writing its outputs and its end state S_start(1); at the same
-//      time every segment p = 1 .. segs-2 runs the transition pass (TRANS,
-//      N = 256) from the augmented state X = [0 | I]: it ends at [B_p | M_p],
-//      the affine map  S_end = M_p S_start + B_p  of the segment;
+//      time every segment p = 1 .. segs-2 runs the transition pass (N = 256)
+//      from the augmented state X = [0 | I]: it ends at [B_p | M_p], the
+//      affine map  S_end = M_p S_start + B_p  of the segment;
 //   launch 2 (phase B): S_start(p+1) = M_p S_start(p) + B_p, sequential over
 //      p >= 1, fp32;
 //   launch 3: segments 1 .. segs-1 run the output pass from their start
 //      states; the last writes the final state.
-// Segment 0 is longer (L0 ~ 1.3 L) because its output pass shares launch 1
-// with the transitions, whose steps take longer.  A sequence that gets one
+// Segment 0 is longer (L0 ~ 1.2 L) because its output pass shares launch 1
+// with the transitions, whose steps take longer (measured: 1.0 and 1.3 were
+// 2% and 3% slower on the chain).  A sequence that gets one
 // segment is the plain chain (launch 1 only).  Planning uses a fixed SM count
 // so that the workspace size depends on (N, H, T) only.
 constexpr int kPlanSMs = 152;
 constexpr int kChainWarps = 16;                 // consumer warps (4 per TMEM lane quarter)
-constexpr int kChainThreads = 32 * kChainWarps + 32;
+constexpr int kChainThreads = 32 * kChainWarps + 32;   // consumers and the record producer
 constexpr int kOLeader = 64;                    // lane 0 of warp 2: issues the output pass's TMA stores
 
 struct ScanPlan {
@@ -726,7 +738,7 @@ struct ScanPlan {
     int segs_max;     // segments of the longest possible sequence
 };
 // Shortest segment, in chunks.  Segments are as long as the SM count allows
-// (2,069 / 1,591 chunks on a 2^20-token sequence of 16 heads); the floor only
+// (1,929 / 1,607 chunks on a 2^20-token sequence of 16 heads); the floor only
 // matters for short sequences, whose walk is a few steps per segment.
 constexpr int64_t kMinSegChunks = 8;
 
@@ -741,9 +753,9 @@ static ScanPlan scan_plan(int N, int H, int64_t T) {
         p.segs_max = 1;
         return p;
     }
-    int64_t len = (10 * chunks_max + 10 * target + 12) / (10 * target + 13);   // chunks_max / (target + 1.3)
+    int64_t len = (10 * chunks_max + 10 * target + 11) / (10 * target + 12);   // chunks_max / (target + 1.2)
     if (len < kMinSegChunks) len = kMinSegChunks;  // below this the launches and the scan cost more than they save
-    int64_t len0 = (13 * len + 9) / 10;
+    int64_t len0 = (12 * len + 9) / 10;
     if (len0 + target * len < chunks_max) len0 = chunks_max - target * len;
     if (len0 > chunks_max) len0 = chunks_max;
     p.len0 = (int)len0;
@@ -770,19 +782,15 @@ size_t tc_extra_bytes(int N, int H, int64_t T) {
     return p.segs_max > 1 ? (size_t)N * H * p.segs_max * kSegBytes : 0;
 }
 
-template <int NX> struct SmemC {
-    static constexpr bool kOut = NX == 128;
-    static constexpr uint32_t kA1 = 0, kKE = 32768, kU0 = 49152, kO0 = 65536;
-    static constexpr uint32_t kGam = kOut ? 81920 : 65536;
-    static constexpr uint32_t kStageUsed = kGam + 512;
-    static constexpr uint32_t kStageBytes = (kStageUsed + 1023) / 1024 * 1024;
-    static constexpr uint32_t kX = 2 * kStageBytes;                 // X operand, MN-major, [128 x NX]
-    static constexpr uint32_t kU = kX + 128 * NX * 2;                // U operand, MN-major, [64 x NX]
-    static constexpr uint32_t kMisc = kOut ? kU + 64 * NX * 2 : kStageUsed;   // TRANS: slack of stage 0
-    static constexpr uint32_t kBytes = kU + 64 * NX * 2 + (kOut ? 256 : 0) + 1024;
-    static constexpr uint32_t kTx = kOut ? kStageUsed : kStageUsed - 16384;   // bytes copied per stage
-    // (the transition copies only the W half of [W; Q']; rows 64..127 of its MMA
-    //  accumulator then hold garbage and are never read)
+// Output pass: a two-stage ring of whole records, the X and U operands.
+struct SmemO {   // byte offsets from a 1024-aligned base
+    static constexpr uint32_t kA1 = 0, kKE = 32768, kU0 = 49152, kO0 = 65536, kGam = 81920;
+    static constexpr uint32_t kTx = kGam + 512;                      // bytes copied per stage
+    static constexpr uint32_t kStageBytes = (kTx + 1023) / 1024 * 1024;
+    static constexpr uint32_t kX = 2 * kStageBytes;                  // X operand, MN-major, [128 x 128]
+    static constexpr uint32_t kU = kX + 128 * 128 * 2;               // U operand, MN-major, [64 x 128]
+    static constexpr uint32_t kMisc = kU + 64 * 128 * 2;
+    static constexpr uint32_t kBytes = kMisc + 256 + 1024;
 };
 
 // Byte offset of (row, col) in an MN-major 128-byte-swizzle operand whose
@@ -808,10 +816,9 @@ struct ChainArgs {
     float* snaps;
 };
 
-// One CTA's pass over segment p of sequence-head blockIdx.x: the output pass
-// (NX = 128) or the transition pass (NX = 256).
-template <int NX>
-__device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
+// One CTA's output pass over segment p of sequence-head blockIdx.x, from the
+// segment's start state: the outputs of its chunks and its end state.
+__device__ __forceinline__ void out_segment(const ChainArgs& A, int p) {
     const int32_t* __restrict__ cu = A.cu;
     DeviceHeader* __restrict__ hdr = A.hdr;
     const int32_t* __restrict__ chunk_first = A.chunk_first;
@@ -823,10 +830,10 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
     uint8_t* __restrict__ segbuf = A.segbuf;
     const int32_t* __restrict__ snap_slot = A.snap_slot;
     float* __restrict__ snaps = A.snaps;
-    using L = SmemC<NX>;
-    constexpr bool kOut = L::kOut;
+    using L = SmemO;
+    constexpr int NX = 128;                            // state columns
     constexpr int kCols = NX / 4;                      // columns per consumer warp
-    constexpr int kLdB = NX == 128 ? 2 : 1;             // TMEM loads in flight per wait (register budget)
+    constexpr int kLdB = 2;                            // TMEM loads in flight per wait
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* full = (uint64_t*)(sm + L::kMisc);     // [2]
@@ -840,7 +847,7 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
     const int nh = blockIdx.x, n = nh / H, h = nh % H;
     const int c_seq = chunk_first[n], nch = chunk_first[n + 1] - c_seq;
     const int segs = seg_count(nch, A.len0, A.len);
-    if (p >= segs || (!kOut && (p == 0 || p >= segs - 1))) return;
+    if (p >= segs) return;
     const int cb = seg_begin(p, A.len0, A.len);                 // chunk range within the sequence
     const int ce = min(nch, seg_begin(p + 1, A.len0, A.len));
     const int nsteps = ce - cb;
@@ -873,29 +880,24 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                 const uint8_t* rec = recs + ((size_t)(c_seq + cb + it) * H + h) * TcRec::kBytes;
                 uint8_t* st = sm + s * L::kStageBytes;
                 mbar_arrive_expect_tx(&full[s], L::kTx);
-                if (kOut) {
-                    bulk_g2s(st + L::kA1, rec + TcRec::kA1, 32768, &full[s]);
-                } else {   // the transition needs W only: rows 0..63 of both K-blocks
-                    bulk_g2s(st + L::kA1, rec + TcRec::kA1, 8192, &full[s]);
-                    bulk_g2s(st + L::kA1 + 16384, rec + TcRec::kA1 + 16384, 8192, &full[s]);
-                }
+                bulk_g2s(st + L::kA1, rec + TcRec::kA1, 32768, &full[s]);
                 bulk_g2s(st + L::kKE, rec + TcRec::kKE, 16384, &full[s]);
                 bulk_g2s(st + L::kU0, rec + TcRec::kU0, 16384, &full[s]);
-                if (kOut) bulk_g2s(st + L::kO0, rec + TcRec::kO0, 16384, &full[s]);
+                bulk_g2s(st + L::kO0, rec + TcRec::kO0, 16384, &full[s]);
                 bulk_g2s(st + L::kGam, rec + TcRec::kGam, 512, &full[s]);
                 issued = it + 1;
             }
             for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
                 mbar_wait(&full[it & 1], (it >> 1) & 1, kWaitNs);
         }
-    } else {
+    } else if (warp < kChainWarps) {
         // ---------------- consumers: rows 32q..32q+31, columns [col0, col0 + kCols) ----------------
         const int q = warp & 3, g = warp >> 2;
         const int i = 32 * q + lane;                 // key channel (row of S / X)
         const int tok = (q & 1) * 32 + lane;          // token row of the U / O halves
         const int col0 = g * kCols;
         float X[kCols];
-        if (kOut) {
+        {
             const float* src = (p == 0) ? initial_state + ((size_t)nh * kTcD + i) * kTcD
                                         : (const float*)(seg + kSegMB) + (size_t)i * kTcD;
             if (p == 0 && !initial_state) {
@@ -908,9 +910,6 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                     X[j] = v.x; X[j + 1] = v.y; X[j + 2] = v.z; X[j + 3] = v.w;
                 }
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < kCols; ++j) X[j] = (col0 + j == kTcD + i) ? 1.f : 0.f;   // [0 | I]
         }
         uint8_t* XO = sm + L::kX;
         uint8_t* UO = sm + L::kU;
@@ -933,8 +932,8 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
         for (int it = 0; it < nsteps && ok; ++it) {
             const int s = it & 1;
             const uint8_t* st = sm + s * L::kStageBytes;
-            // snapshot request for the state after this chunk (output pass only)
-            const int snap_m = (kOut && snap_slot) ? snap_slot[c_seq + cb + it] : -1;
+            // snapshot request for the state after this chunk
+            const int snap_m = snap_slot ? snap_slot[c_seq + cb + it] : -1;
             bool good = mbar_wait(&full[s], (it >> 1) & 1, kWaitNs);
             tc_fence_after_sync();
             if (tid == 0 && good) {
@@ -946,23 +945,29 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                 }
                 mma_commit(mbar);
             }
-            // Output pass: this thread's U0 (U warps) or O0 (O warps) pieces are
-            // read while MMA1 runs (the stage has landed).
-            uint4 pre[kOut ? 4 : 1];
-            if (kOut) {
-                const uint8_t* src = st + (q < 2 ? L::kU0 : L::kO0) + tok * (kTile * 2);
+            // This thread's U0 (U warps) or O0 (O warps) pieces are read while
+            // MMA1 runs (the stage has landed).
+            uint4 pre[4];
+            {
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const uint8_t* p = src + ((col0 + 16 * hh) >> 4) * TcRec::kTileBytes;
-                    pre[2 * hh] = *(const uint4*)p;
-                    pre[2 * hh + 1] = *(const uint4*)(p + 16);
+                    const uint32_t c = (uint32_t)(col0 + 16 * hh);
+                    if (q < 2) {           // U0: two 64-channel blocks, 128-byte swizzle
+                        const uint8_t* ub = st + L::kU0 + (c >> 6) * 8192u;
+                        pre[2 * hh] = *(const uint4*)(ub + sw128_off(tok, c & 63u));
+                        pre[2 * hh + 1] = *(const uint4*)(ub + sw128_off(tok, (c & 63u) + 8u));
+                    } else {               // O0: 16-column tiles
+                        const uint8_t* p = st + L::kO0 + tok * (kTile * 2) + (c >> 4) * TcRec::kTileBytes;
+                        pre[2 * hh] = *(const uint4*)p;
+                        pre[2 * hh + 1] = *(const uint4*)(p + 16);
+                    }
                 }
             }
             good = good && mbar_wait(mbar, ph & 1, kWaitNs);
             ++ph;
             tc_fence_after_sync();
             if (q < 2) {
-                // U = U0 - W X  (the M columns have no U0 term)
+                // U = U0 - W X
 #pragma unroll
                 for (int j2 = 0; j2 < kCols; j2 += 16 * kLdB) {
                   float dd[kLdB][16];
@@ -973,29 +978,17 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                   for (int hh = 0; hh < kLdB; ++hh) {
                     const float (&d)[16] = dd[hh];
                     const int c = col0 + j2 + 16 * hh;
-                    float lo[8], hi[8];
-                    if (c < kTcD) {
-                        float a[8], b[8];
-                        if (kOut) {
-                            unpack8(pre[2 * (j2 / 16 + hh)], a);
-                            unpack8(pre[2 * (j2 / 16 + hh) + 1], b);
-                        } else {
-                            const uint8_t* u0 = st + L::kU0 + (c >> 4) * TcRec::kTileBytes + tok * (kTile * 2);
-                            unpack8(*(const uint4*)u0, a);
-                            unpack8(*(const uint4*)(u0 + 16), b);
-                        }
+                    float lo[8], hi[8], a[8], b[8];
+                    unpack8(pre[2 * (j2 / 16 + hh)], a);
+                    unpack8(pre[2 * (j2 / 16 + hh) + 1], b);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) { lo[e] = a[e] - d[e]; hi[e] = b[e] - d[8 + e]; }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) { lo[e] = -d[e]; hi[e] = -d[8 + e]; }
-                    }
+                    for (int e = 0; e < 8; ++e) { lo[e] = a[e] - d[e]; hi[e] = b[e] - d[8 + e]; }
                     *(uint4*)(UO + mn_off(tok, c, 64)) = pack8(lo);
                     *(uint4*)(UO + mn_off(tok, c + 8, 64)) = pack8(hi);
                   }
                 }
                 fence_proxy_async_smem();
-            } else if (kOut) {
+            } else {
                 // O = O0 + Q' S -> out.  The TMEM loads are warp-collective: every
                 // lane takes part, only the stores of real tokens are predicated.
                 // A full chunk's O goes back into the stage's O0 tiles (same layout
@@ -1033,24 +1026,20 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
                 if (full) fence_proxy_async_smem();
             }
             tc_fence_before_sync();
-            if (kOut) {
-                // MMA3 needs U only: the U warps meet on their own barrier and it
-                // is issued while the O warps finish the outputs (and one of them
-                // issues their TMA stores); everyone meets at the step's end.
-                if (q < 2) {
-                    good = bar_and_id(2, 32 * kChainWarps / 2, good);
-                } else {
-                    good = bar_and_id(3, 32 * kChainWarps / 2, good);
-                    if (tid == kOLeader && good && A.has_tm_out && seq0 + (int64_t)(cb + it + 1) * kChunk <= seq1) {
-#pragma unroll
-                        for (int tl = 0; tl < kTcD / kTile; ++tl)
-                            tma_store_3d(&A.tm_out, st + L::kO0 + tl * TcRec::kTileBytes, tl * kTile, h,
-                                         (int)(seq0 + (int64_t)(cb + it) * kChunk));
-                        bulk_commit();
-                    }
-                }
+            // MMA3 needs U only: the U warps meet on their own barrier and it is
+            // issued while the O warps finish the outputs (and one of them issues
+            // their TMA stores); everyone meets at the step's end.
+            if (q < 2) {
+                good = bar_and_id(2, 32 * kChainWarps / 2, good);
             } else {
-                good = bar_and(32 * kChainWarps, good);
+                good = bar_and_id(3, 32 * kChainWarps / 2, good);
+                if (tid == kOLeader && good && A.has_tm_out && seq0 + (int64_t)(cb + it + 1) * kChunk <= seq1) {
+#pragma unroll
+                    for (int tl = 0; tl < kTcD / kTile; ++tl)
+                        tma_store_3d(&A.tm_out, st + L::kO0 + tl * TcRec::kTileBytes, tl * kTile, h,
+                                     (int)(seq0 + (int64_t)(cb + it) * kChunk));
+                    bulk_commit();
+                }
             }
             tc_fence_after_sync();
             if (tid == 0 && good) {
@@ -1075,14 +1064,14 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) X[j + 16 * hh + e] = fmaf(gam, X[j + 16 * hh + e], d[hh][e]);
             }
-            if (kOut && snap_m >= 0 && good) {
+            if (snap_m >= 0 && good) {
                 float* dst = snaps + (((size_t)snap_m * H + h) * kTcD + i) * kTcD + col0;
 #pragma unroll
                 for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
             }
             write_X(1.f);
             fence_proxy_async_smem();
-            if (kOut && tid == kOLeader) bulk_wait_read_all();   // the stage's O tiles have been stored
+            if (tid == kOLeader) bulk_wait_read_all();   // the stage's O tiles have been stored
             tc_fence_before_sync();
             ok = bar_and(32 * kChainWarps, good);
             if (ok && tid == 0) mbar_arrive(&empty[s]);
@@ -1090,7 +1079,7 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
         if (!ok) {
             *(volatile int*)s_abort = 1;
             if (tid == 0) record_status(hdr, KDA_ERR_TIMEOUT);
-        } else if (kOut) {
+        } else {
             float* dst = nullptr;
             if (p == segs - 1) {
                 if (final_state) dst = final_state + ((size_t)nh * kTcD + i) * kTcD + col0;
@@ -1101,11 +1090,6 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
 #pragma unroll
                 for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
             }
-        } else {
-            // columns 0..127 of X are B_p, 128..255 are M_p
-            float* dst = (float*)(seg + (col0 >= kTcD ? kSegM : kSegB)) + (size_t)i * kTcD + (col0 & (kTcD - 1));
-#pragma unroll
-            for (int j = 0; j < kCols; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
         }
     }
     tc_fence_before_sync();
@@ -1113,18 +1097,257 @@ __device__ __forceinline__ void chain_segment(const ChainArgs& A, int p) {
     if (warp == 0) tmem_dealloc(tmem, 2 * NX);
 }
 
+// Transition pass of segment p (1 .. segs-2) on X = [0 | I] (128 x 256), which
+// ends as [B_p | M_p].  One chunk's step X <- Diag(Gamma) X + K^end^T (U0' - W X),
+// with U0' = [U0 | 0], is written as
+//   X <- Diag(Gamma) X + N X + [B | 0],   N = -K^end^T W,  B = K^end^T U0,
+// so that only the product N X depends on X.  K^end^T [W | U0] of chunk c+1
+// (one MMA group, N = 256, into TMEM columns 256..511) runs on the tensor core
+// right behind N_c X; the consumers then turn its first half into the bf16
+// K-major operand N over the dead W / U0 of that chunk's stage and add
+// Diag(Gamma) X + [B | 0] into the register state, while N_c X is read back.
+// A step is one MMA group (M = 128, N = 256, K = 128) and one pass over the
+// state.  A warp of its own issues the MMAs, so that no consumer warp waits on
+// the tensor core's queue, and the consumer warps hand each step's operands
+// to it through an mbarrier rather than a CTA-wide barrier.
+struct SmemT {   // byte offsets from a 1024-aligned base
+    static constexpr uint32_t kW = 0;            // W, then U0: the B operand [W | U0], MN-major,
+    static constexpr uint32_t kU0 = 16384;       //   4 atoms of [64 tok x 64 ch] at 8 KB (record layouts)
+    static constexpr uint32_t kKE = 32768;       // K^end (record layout): A operand, MN-major
+    static constexpr uint32_t kN = 0;            // then N = -K^end^T W over W / U0: K-major, 2 x [128 x 64]
+    static constexpr uint32_t kGam = 49152;      // Gamma, 128 fp32
+    static constexpr uint32_t kTx = kGam + 512;  // bytes copied per stage
+    static constexpr uint32_t kStageBytes = (kTx + 1023) / 1024 * 1024;
+    static constexpr int kStages = 3;
+    static constexpr uint32_t kX = kStages * kStageBytes;    // X, MN-major [128 x 256] bf16
+    static constexpr uint32_t kMisc = kX + 128 * 256 * 2;
+    static constexpr uint32_t kBytes = kMisc + 128 + 1024;
+};
+constexpr uint32_t kTmD = 0, kTmE = 256, kTmEB = 384;     // TMEM columns: N X; K^end^T W; K^end^T U0
+constexpr int kIssuerWarp = kChainWarps + 1;              // the transition's MMA issuer
+constexpr int kChainFirstThreads = 32 * kChainWarps + 64;  // consumers, producer, issuer
+
+__device__ __forceinline__ void trans_segment(const ChainArgs& A, int p) {
+    using L = SmemT;
+    DeviceHeader* __restrict__ hdr = A.hdr;
+    const int32_t* __restrict__ chunk_first = A.chunk_first;
+    const int H = A.H;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = (uint64_t*)(sm + L::kMisc);     // [kStages]
+    uint64_t* empty = full + L::kStages;             // [kStages]
+    uint64_t* mE = empty + L::kStages;               // K^end^T [W | U0] of a chunk
+    uint64_t* mD = mE + 1;                           // N X of a chunk
+    uint64_t* mC = mD + 1;                           // the consumer warps: a step's operands are in place
+    uint32_t* s_tmem = (uint32_t*)(mC + 1);
+    int* s_abort = (int*)(s_tmem + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (hdr->status != KDA_OK) return;
+    const int nh = blockIdx.x, n = nh / H, h = nh % H;
+    const int c_seq = chunk_first[n], nch = chunk_first[n + 1] - c_seq;
+    const int segs = seg_count(nch, A.len0, A.len);
+    if (p == 0 || p >= segs - 1) return;
+    const int cb = seg_begin(p, A.len0, A.len);
+    const int nsteps = min(nch, seg_begin(p + 1, A.len0, A.len)) - cb;   // >= 1: an inner segment
+    uint8_t* seg = A.segbuf + ((size_t)nh * A.segs_max + p) * kSegBytes;
+
+    if (tid == 0) {
+        for (int s = 0; s < L::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(mE, 1);
+        mbar_init(mD, 1);
+        mbar_init(mC, kChainWarps);
+        fence_mbar_init();
+        *s_abort = 0;
+    }
+    if (warp == 0) { tmem_alloc(s_tmem, 512); tmem_relinquish(); }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *s_tmem;
+    uint8_t* XO = sm + L::kX;
+
+    if (warp == kChainWarps) {
+        // ---------------- producer: W (rows 0..63 of [W; Q']), U0, K^end, Gamma ----------------
+        if (lane == 0) {
+            int issued = 0;
+            for (int it = 0; it < nsteps; ++it) {
+                const int s = it % L::kStages, use = it / L::kStages;
+                if (use >= 1 && !mbar_wait(&empty[s], (use - 1) & 1, kWaitNs)) {
+                    *(volatile int*)s_abort = 1;
+                    break;
+                }
+                if (*(volatile int*)s_abort) break;
+                const uint8_t* rec = A.recs + ((size_t)(c_seq + cb + it) * H + h) * TcRec::kBytes;
+                uint8_t* st = sm + s * L::kStageBytes;
+                mbar_arrive_expect_tx(&full[s], L::kTx);
+                bulk_g2s(st + L::kW, rec + TcRec::kA1, 8192, &full[s]);
+                bulk_g2s(st + L::kW + 8192, rec + TcRec::kA1 + 16384, 8192, &full[s]);
+                bulk_g2s(st + L::kU0, rec + TcRec::kU0, 16384, &full[s]);
+                bulk_g2s(st + L::kKE, rec + TcRec::kKE, 16384, &full[s]);
+                bulk_g2s(st + L::kGam, rec + TcRec::kGam, 512, &full[s]);
+                issued = it + 1;
+            }
+            for (int it = issued - L::kStages < 0 ? 0 : issued - L::kStages; it < issued; ++it)
+                mbar_wait(&full[it % L::kStages], (it / L::kStages) & 1, kWaitNs);
+        }
+    } else if (warp == kIssuerWarp) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            auto issue_E = [&](int it) -> bool {
+                const uint8_t* st = sm + (it % L::kStages) * L::kStageBytes;
+                if (!mbar_wait(&full[it % L::kStages], (it / L::kStages) & 1, kWaitNs)) return false;
+                tc_fence_after_sync();
+                const uint32_t id = idesc_bf16(128, 256, 1, 1);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ss(tmem + kTmE, sdesc(smem_u32(st + L::kKE + ks * 2048), 8192, 1024, 2),
+                                sdesc(smem_u32(st + L::kW + ks * 2048), 8192, 1024, 2), id, ks > 0);
+                mma_commit(mE);
+                return true;
+            };
+            bool good = issue_E(0);
+            for (int it = 0; it < nsteps && good; ++it) {
+                // the consumers have written N_it and X_it and read the accumulators
+                if (!mbar_wait(mC, it & 1, kWaitNs) || *(volatile int*)s_abort) { good = false; break; }
+                tc_fence_after_sync();
+                const uint8_t* st = sm + (it % L::kStages) * L::kStageBytes;
+                const uint32_t id = idesc_bf16(128, 256, 0, 1);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, kin = ks & 3;
+                    mma_bf16_ss(tmem + kTmD, sdesc_k_sw128(smem_u32(st + L::kN + kb * 16384 + kin * 32)),
+                                sdesc(smem_u32(XO + ks * 2048), 16384, 1024, 2), id, ks > 0);
+                }
+                mma_commit(mD);
+                if (it + 1 < nsteps && !issue_E(it + 1)) good = false;
+            }
+            if (!good) *(volatile int*)s_abort = 1;
+        }
+    } else {
+        // ---------------- consumers: row i of X, columns [col0, col0 + 64) ----------------
+        const int q = warp & 3, g = warp >> 2;
+        const int i = 32 * q + lane;
+        const int col0 = g * 64;
+        float X[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) X[j] = (col0 + j == kTcD + i) ? 1.f : 0.f;   // [0 | I]
+        auto write_X = [&]() {
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = X[j + e];
+                *(uint4*)(XO + mn_off(i, col0 + j, 128)) = pack8(v);
+            }
+        };
+        // Once chunk it's K^end^T [W | U0] has landed: N (negated, bf16) over
+        // its stage's dead W / U0, and X <- Diag(Gamma) X + [B | 0] in registers.
+        auto prepare = [&](int it, bool good) -> bool {
+            good = good && mbar_wait(mE, it & 1, kWaitNs);
+            tc_fence_after_sync();
+            uint8_t* st = sm + (it % L::kStages) * L::kStageBytes;
+            {
+                float f0[16], f1[16];
+                tmem_ld16(tmem_addr(tmem, 32 * q, kTmE + 32 * g), f0);
+                tmem_ld16(tmem_addr(tmem, 32 * q, kTmE + 32 * g + 16), f1);
+                tmem_wait_ld();
+                uint8_t* nb = st + L::kN + (uint32_t)(g >> 1) * 16384u;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = -(m < 2 ? f0[8 * m + e] : f1[8 * (m - 2) + e]);
+                    *(uint4*)(nb + sw128_off(i, (uint32_t)(32 * (g & 1) + 8 * m))) = pack8(v);
+                }
+            }
+            const float gam = ((const float*)(st + L::kGam))[i];
+            if (col0 < kTcD) {
+#pragma unroll
+                for (int j = 0; j < 64; j += 32) {
+                    float b0[16], b1[16];
+                    tmem_ld16(tmem_addr(tmem, 32 * q, kTmEB + col0 + j), b0);
+                    tmem_ld16(tmem_addr(tmem, 32 * q, kTmEB + col0 + j + 16), b1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        X[j + e] = fmaf(gam, X[j + e], b0[e]);
+                        X[j + 16 + e] = fmaf(gam, X[j + 16 + e], b1[e]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) X[j] *= gam;
+            }
+            return good;
+        };
+        // This warp's share of a step's operands is in place and its accumulator
+        // reads are done: one arrival per warp.
+        auto hand_off = [&](bool good) {
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (!good) *(volatile int*)s_abort = 1;
+                mbar_arrive(mC);
+            }
+        };
+
+        bool good = true;
+        write_X();
+        good = __all_sync(0xffffffffu, prepare(0, good));
+        hand_off(good);
+        for (int it = 0; it < nsteps && good; ++it) {
+            good = !*(volatile int*)s_abort && mbar_wait(mD, it & 1, kWaitNs);
+            good = __all_sync(0xffffffffu, good);
+            if (!good) break;
+            tc_fence_after_sync();
+            if (tid == 0) mbar_arrive(&empty[it % L::kStages]);   // N_it X_it has read its stage
+#pragma unroll
+            for (int j = 0; j < 64; j += 32) {
+                float d0[16], d1[16];
+                tmem_ld16(tmem_addr(tmem, 32 * q, kTmD + col0 + j), d0);
+                tmem_ld16(tmem_addr(tmem, 32 * q, kTmD + col0 + j + 16), d1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) { X[j + e] += d0[e]; X[j + 16 + e] += d1[e]; }
+            }
+            write_X();
+            if (it + 1 < nsteps) {
+                good = __all_sync(0xffffffffu, prepare(it + 1, good));
+                hand_off(good);
+            }
+        }
+        if (!good) {
+            *(volatile int*)s_abort = 1;
+            if (lane == 0) record_status(hdr, KDA_ERR_TIMEOUT);
+        } else {
+            // columns 0..127 of X are B_p, 128..255 are M_p
+            float* dst = (float*)(seg + (col0 >= kTcD ? kSegM : kSegB)) + (size_t)i * kTcD + (col0 & (kTcD - 1));
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*(volatile int*)s_abort && tid == 0) record_status(hdr, KDA_ERR_TIMEOUT);
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // Launch 1: segment 0's output pass (blockIdx.y == 0) beside the transition
 // passes of segments 1 .. segs-2 (blockIdx.y = p).
-__global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_first(const __grid_constant__ ChainArgs A) {
+__global__ void __launch_bounds__(kChainFirstThreads, 1) kda_tc_chain_first(const __grid_constant__ ChainArgs A) {
     if (A.hdr->status != KDA_OK) return;
-    if (blockIdx.y == 0) chain_segment<128>(A, 0);
-    else chain_segment<256>(A, blockIdx.y);
+    if (blockIdx.y == 0) out_segment(A, 0);
+    else trans_segment(A, blockIdx.y);
 }
+
+constexpr uint32_t kChainFirstSmem = SmemO::kBytes > SmemT::kBytes ? SmemO::kBytes : SmemT::kBytes;
 
 // Launch 3: the output passes of segments 1 .. segs-1 (p = blockIdx.y + 1).
 __global__ void __launch_bounds__(kChainThreads, 1) kda_tc_chain_rest(const __grid_constant__ ChainArgs A) {
     if (A.hdr->status != KDA_OK) return;
-    chain_segment<128>(A, blockIdx.y + 1);
+    out_segment(A, blockIdx.y + 1);
 }
 
 // Phase B: S_start(p+1) = M_p S_start(p) + B_p for p = 1 .. segs-2, from
@@ -1258,9 +1481,9 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
     if ((e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)SmemA::kBytes)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(kda_tc_chain_first, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)SmemC<256>::kBytes)) != cudaSuccess) return e;
+                                  (int)kChainFirstSmem)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(kda_tc_chain_rest, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)SmemC<128>::kBytes)) != cudaSuccess) return e;
+                                  (int)SmemO::kBytes)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(kda_tc_scan_states, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kScanSmem)) != cudaSuccess) return e;
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[0], stream)) != cudaSuccess) return e;
@@ -1290,7 +1513,7 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
     ca.snap_slot = a.snap_slot; ca.snaps = a.snaps;
     const unsigned nh = (unsigned)a.N * a.H;
     const unsigned ylaunch = plan.segs_max > 1 ? (unsigned)plan.segs_max - 1 : 1;
-    kda_tc_chain_first<<<dim3(nh, ylaunch), kChainThreads, SmemC<256>::kBytes, stream>>>(ca);
+    kda_tc_chain_first<<<dim3(nh, ylaunch), kChainFirstThreads, kChainFirstSmem, stream>>>(ca);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (plan.segs_max > 1) {
         if (plan.segs_max > 2) {
@@ -1298,7 +1521,7 @@ cudaError_t prefill_tc_launch(const PrefillArgs& a, int64_t T, cudaStream_t stre
                 a.chunk_first, (DeviceHeader*)a.hdr, a.H, plan.len0, plan.len, ca.segbuf, plan.segs_max);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        kda_tc_chain_rest<<<dim3(nh, ylaunch), kChainThreads, SmemC<128>::kBytes, stream>>>(ca);
+        kda_tc_chain_rest<<<dim3(nh, ylaunch), kChainThreads, SmemO::kBytes, stream>>>(ca);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.phase_events && (e = cudaEventRecord(a.phase_events[2], stream)) != cudaSuccess) return e;
