@@ -1198,7 +1198,7 @@ __device__ __forceinline__ void trans_segment(const ChainArgs& A, int p) {
                 const uint8_t* st = sm + (it % L::kStages) * L::kStageBytes;
                 if (!mbar_wait(&full[it % L::kStages], (it / L::kStages) & 1, kWaitNs)) return false;
                 tc_fence_after_sync();
-                const uint32_t id = idesc_bf16(128, 256, 1, 1);
+                const uint32_t id = idesc_bf16(128, 256, 1, 1) | (1u << 13);   // A negated: [N | -B]
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_ss(tmem + kTmE, sdesc(smem_u32(st + L::kKE + ks * 2048), 8192, 1024, 2),
@@ -1231,7 +1231,7 @@ __device__ __forceinline__ void trans_segment(const ChainArgs& A, int p) {
         const int col0 = g * 64;
         float X[64];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) X[j] = (col0 + j == kTcD + i) ? 1.f : 0.f;   // [0 | I]
+        for (int j = 0; j < 64; ++j) X[j] = (col0 + j == kTcD + i) ? -1.f : 0.f;   // Y = -[0 | I]
         auto write_X = [&]() {
 #pragma unroll
             for (int j = 0; j < 64; j += 8) {
@@ -1257,12 +1257,12 @@ __device__ __forceinline__ void trans_segment(const ChainArgs& A, int p) {
                 for (int m = 0; m < 4; ++m) {
                     float v[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = -(m < 2 ? f0[8 * m + e] : f1[8 * (m - 2) + e]);
+                    for (int e = 0; e < 8; ++e) v[e] = m < 2 ? f0[8 * m + e] : f1[8 * (m - 2) + e];
                     *(uint4*)(nb + sw128_off(i, (uint32_t)(32 * (g & 1) + 8 * m))) = pack8(v);
                 }
             }
             const float gam = ((const float*)(st + L::kGam))[i];
-            if (col0 < kTcD) {
+            if (col0 < kTcD) {           // Y <- Diag(Gamma) Y + (-B)
 #pragma unroll
                 for (int j = 0; j < 64; j += 32) {
                     float b0[16], b1[16];
@@ -1322,10 +1322,10 @@ __device__ __forceinline__ void trans_segment(const ChainArgs& A, int p) {
             *(volatile int*)s_abort = 1;
             if (lane == 0) record_status(hdr, KDA_ERR_TIMEOUT);
         } else {
-            // columns 0..127 of X are B_p, 128..255 are M_p
+            // X = -Y: columns 0..127 are B_p, 128..255 are M_p
             float* dst = (float*)(seg + (col0 >= kTcD ? kSegM : kSegB)) + (size_t)i * kTcD + (col0 & (kTcD - 1));
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) *(float4*)(dst + j) = make_float4(X[j], X[j + 1], X[j + 2], X[j + 3]);
+            for (int j = 0; j < 64; j += 4) *(float4*)(dst + j) = make_float4(-X[j], -X[j + 1], -X[j + 2], -X[j + 3]);
         }
     }
     tc_fence_before_sync();
