@@ -1101,11 +1101,12 @@ __device__ __forceinline__ void out_segment(const ChainArgs& A, int p) {
 // ends as [B_p | M_p].  One chunk's step X <- Diag(Gamma) X + K^end^T (U0' - W X),
 // with U0' = [U0 | 0], is written as
 //   X <- Diag(Gamma) X + N X + [B | 0],   N = -K^end^T W,  B = K^end^T U0,
-// so that only the product N X depends on X.  K^end^T [W | U0] of chunk c+1
-// (one MMA group, N = 256, into TMEM columns 256..511) runs on the tensor core
-// right behind N_c X; the consumers then turn its first half into the bf16
-// K-major operand N over the dead W / U0 of that chunk's stage and add
-// Diag(Gamma) X + [B | 0] into the register state, while N_c X is read back.
+// so that only the product N X depends on X.  -K^end^T [W | U0] = [N | -B] of
+// chunk c+1 (one MMA group, N = 256, A negated, into TMEM columns 256..511)
+// runs on the tensor core right behind N_c X; the consumers then turn its
+// first half into the bf16 K-major operand N over the dead W / U0 of that
+// chunk's stage and fold Diag(Gamma) and -B into the register state, which is
+// carried as Y = -X (Y <- Diag(Gamma) Y + N Y - B; X = -Y at the end).
 // A step is one MMA group (M = 128, N = 256, K = 128) and one pass over the
 // state.  A warp of its own issues the MMAs, so that no consumer warp waits on
 // the tensor core's queue, and the consumer warps hand each step's operands
