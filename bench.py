@@ -91,8 +91,9 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 200):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.path = None
 
@@ -102,7 +103,7 @@ class ClockSampler:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -264,7 +265,7 @@ def run_ours(args, dist: Dist):
 
     phases = [make_events(3) for _ in range(args.steps)]
     t0, t1 = make_events(2)
-    clock = ClockSampler(dev.index)
+    clock = ClockSampler(dev.index, interval_ms=25)     # ~150 ms timed: several samples
     dist.barrier()
     torch.cuda.synchronize()
     clock.start()
@@ -620,7 +621,7 @@ def bench_decode(kda, args, dev, stream, peaks, peak_src):
     torch.cuda.synchronize()
     reps = max(1, args.decode_reps)
     t0, t1 = make_events(2)
-    clock = ClockSampler(dev.index)
+    clock = ClockSampler(dev.index, interval_ms=50)      # the region is ~0.5 s: several samples
     clock.start()
     t0.record(stream)
     for _ in range(reps):
@@ -868,7 +869,7 @@ def main():
     ap.add_argument("--workload", type=int, default=4)
     ap.add_argument("--tokens", type=int, default=0,
                     help="one sequence of this many tokens with the workload's distributions (profiling case)")
-    ap.add_argument("--decode-reps", type=int, default=3)
+    ap.add_argument("--decode-reps", type=int, default=48)   # 48 x 64 steps, ~0.5 s timed
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-pieces", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
