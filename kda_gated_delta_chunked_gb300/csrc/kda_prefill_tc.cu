@@ -112,13 +112,8 @@ __device__ __forceinline__ float ex2_fast(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// Read-only global loads kept in program order (volatile), so they are issued
-// where written even when a later branch could skip their use.
-__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
+// A read-only global load kept in program order (volatile), so that it is
+// issued where written even when a later branch could skip its use.
 __device__ __forceinline__ uint32_t ld_nc_u16(const void* p) {
     unsigned short r;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
