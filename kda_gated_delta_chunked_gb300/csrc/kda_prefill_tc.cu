@@ -53,10 +53,11 @@
 //      reference point in mid-chunk, so that K~ and K^ stay within 2^+-50,
 //      needed a per-channel rescaling in the epilogue and was 5% slower.)
 //   5. The records kernel (b) reads are written as ready-to-copy shared-memory
-//      images: [W; Q'] (K-major, 128-byte swizzle), K^end (token-major), U0 /
-//      O0 in 16-column tiles, Gamma.  [W; Q'] and U0 / O0 are staged in shared
-//      memory (in place over the dead operands) and leave in 1-D bulk stores,
-//      [W; Q'] while the second half of MMA-b runs.  (A coalesced 16-byte copy
+//      images: [W; Q'] (K-major, 128-byte swizzle), K^end and U0 (token-major,
+//      128-byte swizzle), O0 in 16-column tiles (boxes of out), Gamma.  [W; Q']
+//      and U0 / O0 are staged in shared memory (in place over the dead
+//      operands) and leave in 1-D bulk stores, [W; Q'] while the second half of
+//      MMA-b runs.  (A coalesced 16-byte copy
 //      by all threads was 4% slower, and stores straight from the accumulator
 //      rows, where every lane of a store touched its own 128-byte line, 9%.)
 // Chunks whose cumulative decay from the chunk start exceeds 2^100 in some
