@@ -1120,7 +1120,7 @@ struct SmemT {   // byte offsets from a 1024-aligned base
     static constexpr uint32_t kMisc = kX + 128 * 256 * 2;
     static constexpr uint32_t kBytes = kMisc + 128 + 1024;
 };
-constexpr uint32_t kTmD = 0, kTmE = 256, kTmEB = 384;     // TMEM columns: N X; K^end^T W; K^end^T U0
+constexpr uint32_t kTmD = 0, kTmE = 256, kTmEB = 384;     // TMEM columns: N X; N = -K^end^T W; -B = -K^end^T U0
 constexpr int kIssuerWarp = kChainWarps + 1;              // the transition's MMA issuer
 constexpr int kChainFirstThreads = 32 * kChainWarps + 64;  // consumers, producer, issuer
 
@@ -1222,7 +1222,8 @@ __device__ __forceinline__ void trans_segment(const ChainArgs& A, int p) {
             if (!good) *(volatile int*)s_abort = 1;
         }
     } else {
-        // ---------------- consumers: row i of X, columns [col0, col0 + 64) ----------------
+        // ---------------- consumers: row i of the state, columns [col0, col0 + 64) ----------------
+        // (X[] holds Y = -X; the MMA operand written from it is Y as well)
         const int q = warp & 3, g = warp >> 2;
         const int i = 32 * q + lane;
         const int col0 = g * 64;
